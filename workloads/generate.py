@@ -1,0 +1,67 @@
+"""Draw the seeded weights and gradients of a `Workload` with torch.
+
+Each tensor gets its own generator, seeded from (workload seed, kind, step,
+tensor index), so a tensor's values do not depend on which other tensors are
+drawn or in which order.  Values drawn on the CPU and on a CUDA device differ
+(different generators); every consumer copies the values it needs from the
+tensors actually used, never re-draws them.
+"""
+from __future__ import annotations
+
+import hashlib
+
+import torch
+
+from .configs import BF16, F32, Workload
+
+_DTYPES = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+def torch_dtype(tag: str) -> torch.dtype:
+    return _DTYPES[tag]
+
+
+def tensor_seed(seed: int, kind: str, step: int, index: int) -> int:
+    h = hashlib.sha256(f"{seed}/{kind}/{step}/{index}".encode()).digest()
+    return int.from_bytes(h[:8], "little") & ((1 << 63) - 1)
+
+
+def _normal(shape, std: float, seed: int, device, dtype) -> torch.Tensor:
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    x.mul_(std)
+    return x if dtype == torch.float32 else x.to(dtype)
+
+
+def draw_params(w: Workload, device="cpu") -> list:
+    """fp32 weights N(0, param_std) for every tensor, frozen ones included."""
+    return [_normal(t.shape, w.param_std, tensor_seed(w.seed, "param", 0, i), device, torch.float32)
+            for i, t in enumerate(w.tensors)]
+
+
+def draw_grads(w: Workload, step: int, device="cpu", out=None) -> list:
+    """Gradients of step `step` (1-based) in each tensor's grad dtype,
+    N(0, grad_std), zeros for tensors flagged zero_grad.  Frozen tensors get
+    gradients too, so that a test can check nobody reads or writes them.
+    With `out`, values are written into those tensors instead."""
+    res = []
+    for i, t in enumerate(w.tensors):
+        dt = _DTYPES[t.grad_dtype]
+        if t.zero_grad:
+            g = torch.zeros(t.shape, device=device, dtype=dt)
+        else:
+            g = _normal(t.shape, w.grad_std, tensor_seed(w.seed, "grad", step, i), device, dt)
+        if out is not None:
+            out[i].copy_(g)
+            del g
+            res.append(out[i])
+        else:
+            res.append(g)
+    return res
+
+
+def zero_moments(w: Workload, device="cpu"):
+    m = [torch.zeros(t.shape, device=device, dtype=torch.float32) for t in w.tensors]
+    v = [torch.zeros(t.shape, device=device, dtype=torch.float32) for t in w.tensors]
+    return m, v
