@@ -93,10 +93,13 @@ double oracle_global_norm(const oracle_tensor *ts, int64_t n, double divisor)
     return sqrt(total);
 }
 
-/* Clip coefficient (step 3). */
+/* Clip coefficient (step 3).  A NaN norm gives a NaN coefficient, as
+ * clip_grad_norm_'s clamp does; an infinite norm gives 0. */
 double oracle_clip_coef(double norm, double max_norm)
 {
     double c = max_norm / (norm + 1e-6);
+    if (isnan(c))
+        return c;
     return c < 1.0 ? c : 1.0;
 }
 

@@ -314,3 +314,27 @@ def test_matches_torch_library_special_case(divisor, max_norm, grad_scale):
             np.testing.assert_allclose(opt.exp_avg_sq[k], ref_v[k], rtol=1e-11, atol=1e-24)
         else:
             assert np.array_equal(opt.params[k], params[k])
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_nonfinite_gradient_follows_the_library(bad):
+    # Not covered by the pages; the reading is clip_grad_norm_'s default
+    # (no error): a NaN norm propagates into every update, an infinite norm
+    # gives c = 0.
+    rng = np.random.default_rng(31)
+    sizes = (9, 4)
+    params = [rng.standard_normal(n) * 0.02 for n in sizes]
+    flags = [(0, True, True), (0, True, True)]
+    grads = [f32(rng.standard_normal(n)) for n in sizes]
+    grads[1][2] = bad
+    groups = [GroupState(lr=1e-3, weight_decay=0.01)]
+    ref_p, ref_m, ref_v, ref_norms = _torch_reference_run(params, [grads], flags, groups, 2.0, 1.0, [(1e-3,)])
+    opt = OracleOptimizer(params, flags, [GroupState(**vars(g)) for g in groups])
+    norm, c = opt.step(grads, 2.0, 1.0)
+    if bad != bad:
+        assert math.isnan(norm) and math.isnan(c)
+    else:
+        assert norm == float("inf") and c == 0.0
+    for k in range(2):
+        np.testing.assert_allclose(opt.params[k], ref_p[k], rtol=1e-12, equal_nan=True)
+        np.testing.assert_allclose(opt.exp_avg[k], ref_m[k], rtol=1e-12, equal_nan=True)
