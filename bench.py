@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Throughput of the fused normalize -> global-norm clip -> AdamW step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload action_expert|hsdp_shard|flat|many_small|tiny]
+
+A step is one soma_opt_step over the whole tensor list (square-sum kernel +
+fused update kernel).  Default workload: the 18-block action-expert list
+(302,008,320 fp32 parameters, bf16 gradients, 144 tensors, 2 groups,
+divisor 64, max_norm 1).  Inputs are synthetic and resident in HBM; p, m and v
+are 1.2 GB each, far above the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0): value = trainable parameter elements updated
+per second over all ranks, plus the effective HBM bandwidth under the stated
+accounting (28 B per element with bf16 gradients, 32 B with fp32), a
+roofline entry for the update kernel, the oracle's CPU throughput, an
+end-to-end number through the C ABI with host-resident gradients, and the SM
+clocks seen during the timed region.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this step available here) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "param-elements updated/sec and effective HBM GB/s (% of GB300 peak) per step"
+UNIT = "param-elements/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+PROFILE_JSON = os.path.join(ROOT, "profiles", "update_kernel_action_expert.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="action_expert")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tuning", default="", help="update_chunk,norm_chunk,ctas_per_sm")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback", {}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index = index
+        self.period = period_ms
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period)], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for nm, val in zip(names, r[5:9]):
+                    if val.strip() == "Active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload(name):
+    import workloads as W
+    if name not in W.FULL:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.FULL)}")
+    return W.FULL[name]()
+
+
+def describe(w):
+    import workloads as W
+    dts = sorted({t.grad_dtype for t in w.tensors if t.trainable})
+    return {
+        "workload": f"{w.name}: {len(w.tensors)} tensors, {w.trainable_numel:,} trainable fp32 params, "
+                    f"{'/'.join(dts)} grads, {len(w.groups)} groups, divisor {w.grad_divisor:g}, "
+                    f"max_norm {w.max_norm:g}",
+        "tensors": len(w.tensors),
+        "trainable_params": w.trainable_numel,
+        "owned_params": w.owned_numel,
+        "grad_dtype": "/".join(dts),
+        "effective_bytes_per_step": w.effective_bytes_per_step(),
+        "algorithmic_bytes_per_step": w.algorithmic_bytes_per_step(),
+        "l2": "no flush: p, m, v and g exceed the 129 MB L2" if w.trainable_numel * 4 > 4 * L2_BYTES
+        else "working set may fit in L2 (small workload)",
+    }
+
+
+def alloc_flat(w, device):
+    """One flat device buffer per kind (p, g, m, v); each tensor is a view
+    starting on a 256-byte boundary.  Weights and gradients drawn on device."""
+    import torch
+    import workloads as W
+    offs, cur = [], 0
+    for t in w.tensors:
+        offs.append(cur)
+        cur += (t.numel + 63) // 64 * 64
+    total = max(cur, 64)
+    gdt = {W.torch_dtype(t.grad_dtype) for t in w.tensors}
+    if len(gdt) != 1:
+        raise SystemExit("bench expects one gradient dtype per workload")
+    gdt = gdt.pop()
+    P = torch.empty(total, dtype=torch.float32, device=device)
+    G = torch.zeros(total, dtype=gdt, device=device)
+    M = torch.zeros(total, dtype=torch.float32, device=device)
+    V = torch.zeros(total, dtype=torch.float32, device=device)
+    p, g, m, v = [], [], [], []
+    for k, t in enumerate(w.tensors):
+        sl = slice(offs[k], offs[k] + t.numel)
+        p.append(P[sl]); g.append(G[sl]); m.append(M[sl]); v.append(V[sl])
+        p[-1].copy_(W.draw_param(w, k, device).reshape(-1))
+        g[-1].copy_(W.draw_grad(w, k, 1, device).reshape(-1))
+    return (P, G, M, V), (p, g, m, v)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "soma_kernels.h"):
+        with open(os.path.join(ROOT, "tensor_grad_clip_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name):
+    """DRAM bytes per update-kernel launch from the committed ncu summary,
+    if it was taken on this workload and on the current kernel source."""
+    try:
+        with open(PROFILE_JSON) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_sha") != kernel_source_hash() or d.get("workload") != workload_name:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(w, budget_s=10.0):
+    """The fp64 oracle (single thread, as it stands) on the first tensors of
+    the workload, repeated until about `budget_s` seconds have passed."""
+    import oracle
+    import workloads as W
+    from oracle import GroupState, OracleOptimizer
+    oracle.lib()
+    idx, n = [], 0
+    for k, t in enumerate(w.tensors):
+        if t.trainable and n < 8_500_000:
+            idx.append(k)
+            n += t.numel
+    params = [W.draw_param(w, k, "cpu") for k in idx]
+    grads = [W.draw_grad(w, k, 1, "cpu") for k in idx]
+    orc = OracleOptimizer([p.double().numpy().reshape(-1) for p in params],
+                          [(w.tensors[k].group, True, w.tensors[k].owned) for k in idx],
+                          [GroupState(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                                      weight_decay=g.weight_decay) for g in w.groups])
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        orc.step(grads, w.grad_divisor, w.max_norm)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": n * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(idx)} tensors ({n:,} params) of {w.name}, {steps} full oracle steps "
+                      f"(norm + update) in {el:.1f} s, fp64, one thread"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: K timed steps after W warm-ups, each
+    a bounded sample of the workload, sized to finish within minutes."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import workloads as W
+    from oracle import GroupState, OracleOptimizer
+    w = workload(args.workload)
+    oracle.lib()
+    # calibrate: elements per second on one tensor, then size the per-step sample
+    k0 = next(k for k, t in enumerate(w.tensors) if t.trainable)
+    cal_p = W.draw_param(w, k0, "cpu")
+    cal_g = W.draw_grad(w, k0, 1, "cpu")
+    cal = OracleOptimizer([cal_p.double().numpy().reshape(-1)], [(w.tensors[k0].group, True, True)],
+                          [GroupState(lr=g.lr) for g in w.groups])
+    t0 = time.perf_counter()
+    cal.step([cal_g], w.grad_divisor, w.max_norm)
+    rate = cal_p.numel() / max(time.perf_counter() - t0, 1e-6)
+    per_step = min(17_000_000, max(1, int(rate * 120.0 / max(1, args.steps + args.warmup))))
+    idx, n = [], 0
+    for k, t in enumerate(w.tensors):
+        if t.trainable and (n == 0 or n + t.numel <= per_step):
+            idx.append(k)
+            n += t.numel
+    params = [W.draw_param(w, k, "cpu") for k in idx]
+    grads = [W.draw_grad(w, k, 1, "cpu") for k in idx]
+    orc = OracleOptimizer([p.double().numpy().reshape(-1) for p in params],
+                          [(w.tensors[k].group, True, w.tensors[k].owned) for k in idx],
+                          [GroupState(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                                      weight_decay=g.weight_decay) for g in w.groups])
+    for _ in range(args.warmup):
+        orc.step(grads, w.grad_divisor, w.max_norm)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.step(grads, w.grad_divisor, w.max_norm)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": describe(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{len(idx)} tensors ({n:,} params) of {w.name} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from tensor_grad_clip_gb300 import SomaOpt, TensorList
+    import tensor_grad_clip_gb300
+    tensor_grad_clip_gb300.load()
+
+    w = workload(args.workload)
+    flats, (p, g, m, v) = alloc_flat(w, device)
+    opt = SomaOpt(local)
+    for q in w.groups:
+        opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+    if args.tuning:
+        uc, nc, cps = (int(x) for x in args.tuning.split(","))
+        opt.set_tuning(uc, nc, cps)
+    tl = TensorList(p, g, m, v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
+                    owned=[t.owned for t in w.tensors])
+    stream = torch.cuda.current_stream(device)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        lrs = w.group_lrs(i + 1)
+        for q, lr in enumerate(lrs):
+            opt.set_lr(q, lr)
+        opt.step(tl, w.grad_divisor, w.max_norm, stream)
+    torch.cuda.synchronize()
+    plan = opt.plan()
+    opt.set_timing(True)
+    opt.read_timing()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        if w.lr_at is not None:
+            for q, lr in enumerate(w.group_lrs(i % w.steps + 1)):
+                opt.set_lr(q, lr)
+        opt.step(tl, w.grad_divisor, w.max_norm, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    norm_ms, upd_ms, nsteps = opt.read_timing()
+    opt.set_timing(False)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    norm, coef, nonfinite = opt.get_norm(stream)
+
+    ms_per_step = elapsed_ms / args.steps
+    elems = w.trainable_numel
+    value = elems * world * args.steps / (elapsed_ms / 1e3)
+    hbm_peak, peak_kind, _ = peaks()
+    eff_gbs = w.effective_bytes_per_step() / (ms_per_step / 1e3) / 1e9
+    alg_gbs = w.algorithmic_bytes_per_step() / (ms_per_step / 1e3) / 1e9
+
+    # dominant kernel: the fused update (26 B/elem bf16 grads, 28 B/elem fp32)
+    upd_bytes = sum(t.numel * ((2 if t.grad_dtype == "bf16" else 4) + 24) for t in w.tensors if t.trainable)
+    norm_bytes = sum(t.numel * (2 if t.grad_dtype == "bf16" else 4) for t in w.tensors if t.trainable and t.owned)
+    upd_avg_ms = upd_ms / max(nsteps, 1)
+    norm_avg_ms = norm_ms / max(nsteps, 1)
+    achieved = upd_bytes / (upd_avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "update_kernel", "achieved": achieved, "peak": hbm_peak,
+                "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                "traffic": ncu_traffic(w.name), "algorithmic_bytes_per_launch": upd_bytes,
+                "avg_launch_ms": upd_avg_ms,
+                "norm_kernel": {"achieved": norm_bytes / (norm_avg_ms / 1e3) / 1e9 if norm_avg_ms > 0 else None,
+                                "avg_launch_ms": norm_avg_ms, "algorithmic_bytes_per_launch": norm_bytes}}
+
+    e2e = None
+    if not args.no_e2e:
+        # End to end through the C ABI: every step copies that step's gradients
+        # from pinned host memory and reads the norm back.
+        G = flats[1]
+        host_g = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+        host_g.copy_(G)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            G.copy_(host_g, non_blocking=True)
+            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+            opt.get_norm(stream)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            G.copy_(host_g, non_blocking=True)
+            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+            opt.get_norm(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - t0
+        e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": elems * world * args.e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": 48,
+               "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": describe(w) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                     "plan": plan},
+            "effective_hbm_gbs": eff_gbs * world,
+            "effective_hbm_frac_of_peak": eff_gbs / hbm_peak,
+            "effective_hbm_frac_of_8tbs": eff_gbs / 8000.0,
+            "algorithmic_hbm_gbs": alg_gbs * world,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": plan["launches_per_step"] * args.steps,
+            "clocks": clocks,
+            "last_norm": norm, "last_clip_coef": coef, "nonfinite": nonfinite,
+        }
+        print(json.dumps(line), flush=True)
+    opt.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * soma_opt.h -- C ABI of the fused "normalize -> global-norm clip -> AdamW"
+ * optimizer step for GB300 (sm_103a).
+ *
+ * What one step computes (SomaSpeed page, "Robot learning, at a different
+ * pace", optimizer paragraphs "After backward, each trainable tensor has a
+ * gradient ..." and "SomaSpeed batches that work across tensors ..."):
+ *
+ *   over a list of tensors, with d = grad_divisor,
+ *     norm = sqrt( sum over trainable, owned tensors of sum_i (g_i / d)^2 )
+ *     c    = min(1, max_norm / (norm + 1e-6))
+ *   then, for every element of every trainable tensor (owned or not),
+ *     g' = g * c / d
+ *     p  = p * (1 - lr * wd)
+ *     m  = b1 * m + (1 - b1) * g'
+ *     v  = b2 * v + (1 - b2) * g'^2
+ *     p  = p - (lr / bc1) * m / (sqrt(v) / sqrt(bc2) + eps),   bc_k = 1 - b_k^t
+ *   with lr, b1, b2, eps, wd and the step count t of the tensor's group.
+ *
+ * The coefficient is that of torch.nn.utils.clip_grad_norm_ with the L2 norm,
+ * which the veRL write-up calls before optimizer.step() ("veRL Training
+ * Process", 4.2 PPO Update; max_norm 1.0 in "PPO Update Summary").  The
+ * update is torch.optim.AdamW (decoupled decay, bias correction, eps outside
+ * the square root).  Gradients may be bf16 on fp32 weights and moments; they
+ * are widened to fp32 for the update (RLinf, "Adding New Models with
+ * FSDP+HuggingFace", "Retaining Low-Precision Gradients").  Gradient buffers
+ * are only read; frozen tensors are neither read nor written.
+ *
+ * Ownership of memory: every tensor buffer and the stream belong to the
+ * caller; the library never frees them.  The library owns its handle and the
+ * device memory behind it (tensor/chunk tables, per-chunk partial sums, the
+ * norm/coefficient result) and frees it in soma_opt_destroy.
+ *
+ * Errors: every call returns a status; nothing aborts or exits.  All
+ * argument checks run before any state change or launch, so a call that
+ * returns an error other than SOMA_ERR_CUDA has changed nothing.
+ * soma_opt_last_error() gives the detail text of the last failure.
+ *
+ * Threads: a handle may be used by one thread at a time.  Distinct handles
+ * are independent.
+ *
+ * Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy
+ * default stream).
+ */
+#ifndef SOMA_OPT_H
+#define SOMA_OPT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+typedef int32_t soma_status_t;
+#define SOMA_OK               0
+#define SOMA_ERR_INVALID_ARG  1  /* null pointer, negative size, bad flag, non-finite or out-of-range value */
+#define SOMA_ERR_BAD_GROUP    2  /* group id not returned by soma_opt_add_group */
+#define SOMA_ERR_DTYPE        3  /* unknown gradient dtype code */
+#define SOMA_ERR_ALIGNMENT    4  /* buffer not aligned to its element size */
+#define SOMA_ERR_OOM          5  /* device or pinned host allocation failed */
+#define SOMA_ERR_CUDA         6  /* a CUDA runtime call failed (detail in soma_opt_last_error) */
+#define SOMA_ERR_STATE        7  /* null or destroyed handle */
+#define SOMA_ERR_LIMIT        8  /* more groups than SOMA_MAX_GROUPS */
+
+/* ---- gradient dtypes --------------------------------------------------- */
+#define SOMA_DTYPE_F32   0  /* IEEE binary32 */
+#define SOMA_DTYPE_BF16  1  /* bfloat16: the upper 16 bits of a binary32 */
+
+#define SOMA_MAX_GROUPS  64
+#define SOMA_ABI_VERSION 1
+
+typedef struct soma_opt soma_opt;
+typedef soma_opt *soma_opt_t;
+
+/* One entry of the tensor list (48 bytes, no implicit padding).
+ * All buffers are contiguous 1-D views of `numel` elements in device memory
+ * (torch's Tensor.data_ptr() of a contiguous tensor).
+ *   param       fp32 weights, updated in place; 4-byte aligned.
+ *   grad        gradient in grad_dtype; NEVER written; aligned to its element size.
+ *   exp_avg     fp32 first moment m, updated in place (zeros before step 1).
+ *   exp_avg_sq  fp32 second moment v, updated in place (zeros before step 1).
+ *   numel       >= 0.
+ *   group       id from soma_opt_add_group; ignored when frozen.
+ *   grad_dtype  SOMA_DTYPE_*; ignored when frozen.
+ *   trainable   0 = frozen: never read, never written, not in the norm; its
+ *               pointers may be NULL.  1 = trainable.
+ *   owned       1 = this rank owns the tensor (shard): it enters the norm.
+ *               0 = replicated copy: updated with the same c, not in the norm.
+ *   reserved    must be 0.
+ * Buffers of different entries, and param/grad/exp_avg/exp_avg_sq of one
+ * entry, must not overlap. */
+typedef struct {
+    float *param;
+    const void *grad;
+    float *exp_avg;
+    float *exp_avg_sq;
+    int64_t numel;
+    int32_t group;
+    uint8_t grad_dtype;
+    uint8_t trainable;
+    uint8_t owned;
+    uint8_t reserved;
+} soma_tensor_t;
+
+/* Create a handle bound to CUDA device `device`.  Makes no CUDA call: device
+ * memory is allocated on the first step.  *out is set to NULL on failure. */
+soma_status_t soma_opt_create(soma_opt_t *out, int32_t device);
+
+/* Add a parameter group with torch.optim.AdamW's hyperparameters
+ * (lr >= 0, 0 <= beta1, beta2 < 1, eps > 0, weight_decay >= 0, all finite).
+ * Its step count starts at 0.  Writes the new id (0, 1, ...) to *group_id. */
+soma_status_t soma_opt_add_group(soma_opt_t opt, double lr, double beta1, double beta2,
+                                 double eps, double weight_decay, int32_t *group_id);
+
+/* Change a group's lr (learning-rate schedules); applies to the next step. */
+soma_status_t soma_opt_set_lr(soma_opt_t opt, int32_t group, double lr);
+
+/* Read or replace all hyperparameters of a group (same ranges as add_group). */
+soma_status_t soma_opt_get_group(soma_opt_t opt, int32_t group, double *lr, double *beta1,
+                                 double *beta2, double *eps, double *weight_decay);
+soma_status_t soma_opt_set_group(soma_opt_t opt, int32_t group, double lr, double beta1,
+                                 double beta2, double eps, double weight_decay);
+
+/* Step count of a group (checkpoint and resume).  set: t >= 0. */
+soma_status_t soma_opt_get_group_step(soma_opt_t opt, int32_t group, int64_t *t);
+soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
+
+/* One optimizer step over `list[0..n)` (n >= 0; list may be NULL when n == 0),
+ * with effective-batch divisor grad_divisor > 0 and max_norm > 0, both
+ * finite.  Each group with at least one trainable entry in the list advances
+ * its step count by one.  Enqueues two kernels on `stream` and returns without
+ * waiting for them: the owned square-sum (which also derives norm and c on
+ * the device) and the fused update.  No device-to-host synchronisation
+ * happens, except that a list differing from the previous call's waits for
+ * the previous step's kernels before the device tables are rewritten. */
+soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
+                            double grad_divisor, double max_norm, void *stream);
+
+/* Norm and clip coefficient of the last step (fp64), and 1 if that norm was
+ * not finite.  Any output pointer may be NULL.  Waits for the last step on
+ * `stream`: the only call besides soma_opt_read_timing that blocks. */
+soma_status_t soma_opt_get_norm(soma_opt_t opt, double *norm, double *clip_coef,
+                                int32_t *nonfinite, void *stream);
+
+/* Kernel timing: when enabled, each step records CUDA events around its two
+ * kernels on the step's stream.  read_timing waits for them and returns the
+ * summed kernel times (ms) and the number of steps since the last read. */
+soma_status_t soma_opt_set_timing(soma_opt_t opt, int32_t enable);
+soma_status_t soma_opt_read_timing(soma_opt_t opt, double *norm_ms, double *update_ms,
+                                   int64_t *steps);
+
+/* Launch plan of the last step: chunk and segment counts, grid and block
+ * sizes of the square-sum and update kernels.  Any pointer may be NULL. */
+typedef struct {
+    int64_t norm_chunks, norm_segments, update_chunks, update_segments;
+    int32_t norm_grid, norm_block, update_grid, update_block;
+    int64_t trainable_numel, owned_numel;
+    int32_t launches_per_step;
+    int32_t reserved;
+} soma_plan_t;
+soma_status_t soma_opt_get_plan(soma_opt_t opt, soma_plan_t *plan);
+
+/* Tuning knobs for benchmarks: elements per update chunk and per norm chunk
+ * (rounded to a multiple of 64; 0 keeps the default) and resident CTAs per
+ * SM for a persistent grid (0 = one CTA per chunk).  Takes effect at the next
+ * list (re)build. */
+soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t norm_chunk,
+                                  int32_t ctas_per_sm);
+
+/* Text of a status code (static storage). */
+const char *soma_status_string(soma_status_t status);
+
+/* Detail of the last failure on `opt` (or, for opt == NULL, of the calling
+ * thread's last failed soma_opt_create).  Valid until the next call on it. */
+const char *soma_opt_last_error(soma_opt_t opt);
+
+/* SOMA_ABI_VERSION of the loaded library. */
+int32_t soma_abi_version(void);
+
+/* Wait for the handle's outstanding work, free its device and host memory
+ * and the handle.  NULL is ignored. */
+void soma_opt_destroy(soma_opt_t opt);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SOMA_OPT_H */

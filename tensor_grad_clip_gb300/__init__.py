@@ -1,0 +1,199 @@
+"""GB300-native fused optimizer step: normalize gradients by the effective
+batch, one global L2 norm over owned shards, one clip coefficient, and
+AdamW on fp32 weights and moments, in two sm_103a kernels behind a C ABI
+(include/soma_opt.h).
+
+This module only marshals arguments for that ABI; torch supplies device
+memory and streams.  Typical use::
+
+    opt = SomaOpt(device=0)
+    g_mat = opt.add_group(lr=5e-6, weight_decay=0.01)
+    tl = TensorList(params, grads, exp_avgs, exp_avg_sqs, groups=[g_mat, ...])
+    opt.step(tl, grad_divisor=64.0, max_norm=1.0)      # async on the current stream
+    norm, coef, nonfinite = opt.get_norm()            # waits
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+from . import _abi
+from ._abi import (SOMA_DTYPE_BF16, SOMA_DTYPE_F32, SOMA_MAX_GROUPS, soma_plan_t,  # noqa: F401
+                   soma_tensor_t)
+
+__all__ = ["SomaOpt", "TensorList", "SomaError", "load", "soma_tensor_t", "soma_plan_t"]
+
+
+def load():
+    return _abi.load()
+
+
+class SomaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def _grad_code(dtype) -> int:
+    import torch
+    if dtype == torch.float32:
+        return SOMA_DTYPE_F32
+    if dtype == torch.bfloat16:
+        return SOMA_DTYPE_BF16
+    raise TypeError(f"unsupported gradient dtype {dtype} (float32 or bfloat16)")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class TensorList:
+    """The soma_tensor_t array for lists of torch tensors, built once and
+    reused every step (the tensors must stay alive and keep their storage).
+
+    params / exp_avgs / exp_avg_sqs: contiguous float32 tensors.
+    grads: contiguous float32 or bfloat16 tensors (never written).
+    groups: group id per tensor.  trainable / owned: bools per tensor
+    (default all True).  Frozen entries may pass None buffers."""
+
+    def __init__(self, params: Sequence, grads: Sequence, exp_avgs: Sequence, exp_avg_sqs: Sequence,
+                 groups: Sequence[int], trainable: Optional[Sequence[bool]] = None,
+                 owned: Optional[Sequence[bool]] = None):
+        import torch
+        n = len(params)
+        if not (len(grads) == len(exp_avgs) == len(exp_avg_sqs) == len(groups) == n):
+            raise ValueError("all per-tensor sequences must have the same length")
+        trainable = [True] * n if trainable is None else list(trainable)
+        owned = [True] * n if owned is None else list(owned)
+        self.n = n
+        self.array = (soma_tensor_t * max(n, 1))()
+        self.tensors = list(zip(params, grads, exp_avgs, exp_avg_sqs))  # keep alive
+
+        def ptr(t, dtype=None):
+            if t is None:
+                return None
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+            if dtype is not None and t.dtype != dtype:
+                raise TypeError(f"expected {dtype}, got {t.dtype}")
+            return t.data_ptr()
+
+        for k, (p, g, m, v) in enumerate(self.tensors):
+            tr = bool(trainable[k])
+            e = self.array[k]
+            numel = p.numel() if p is not None else (g.numel() if g is not None else 0)
+            if tr:
+                for other in (g, m, v):
+                    if other is None or other.numel() != numel:
+                        raise ValueError(f"tensor {k}: param, grad, exp_avg, exp_avg_sq must have equal numel")
+            e.param = ptr(p, torch.float32)
+            e.grad = ptr(g)
+            e.exp_avg = ptr(m, torch.float32)
+            e.exp_avg_sq = ptr(v, torch.float32)
+            e.numel = numel
+            e.group = int(groups[k])
+            e.grad_dtype = _grad_code(g.dtype) if (tr and g is not None) else 0
+            e.trainable = 1 if tr else 0
+            e.owned = 1 if owned[k] else 0
+            e.reserved = 0
+
+    def pointer(self):
+        return ctypes.cast(self.array, ctypes.POINTER(soma_tensor_t))
+
+
+class SomaOpt:
+    """A handle of the C library (soma_opt_create ... soma_opt_destroy)."""
+
+    def __init__(self, device: int = 0):
+        self._lib = _abi.load()
+        h = _abi.soma_opt_t()
+        st = _abi.soma_opt_create(ctypes.byref(h), int(device))
+        if st != 0:
+            raise SomaError(st, _abi.soma_opt_last_error(None).decode())
+        self._h = h
+        self.device = int(device)
+
+    def _check(self, st: int):
+        if st != 0:
+            raise SomaError(st, _abi.soma_opt_last_error(self._h).decode())
+
+    @property
+    def handle(self):
+        return self._h
+
+    def add_group(self, lr: float, betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0) -> int:
+        gid = ctypes.c_int32()
+        self._check(_abi.soma_opt_add_group(self._h, lr, betas[0], betas[1], eps, weight_decay,
+                                            ctypes.byref(gid)))
+        return gid.value
+
+    def set_lr(self, group: int, lr: float):
+        self._check(_abi.soma_opt_set_lr(self._h, group, lr))
+
+    def get_group(self, group: int) -> dict:
+        vals = [ctypes.c_double() for _ in range(5)]
+        self._check(_abi.soma_opt_get_group(self._h, group, *[ctypes.byref(v) for v in vals]))
+        lr, b1, b2, eps, wd = (v.value for v in vals)
+        return dict(lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd)
+
+    def set_group(self, group: int, lr: float, betas=(0.9, 0.999), eps: float = 1e-8,
+                  weight_decay: float = 0.0):
+        self._check(_abi.soma_opt_set_group(self._h, group, lr, betas[0], betas[1], eps, weight_decay))
+
+    def get_group_step(self, group: int) -> int:
+        t = ctypes.c_int64()
+        self._check(_abi.soma_opt_get_group_step(self._h, group, ctypes.byref(t)))
+        return t.value
+
+    def set_group_step(self, group: int, t: int):
+        self._check(_abi.soma_opt_set_group_step(self._h, group, t))
+
+    def step(self, tensors: TensorList, grad_divisor: float, max_norm: float, stream=None):
+        self._check(_abi.soma_opt_step(self._h, tensors.pointer(), tensors.n, grad_divisor, max_norm,
+                                       _stream_handle(stream)))
+
+    def get_norm(self, stream=None):
+        """(norm, clip_coef, nonfinite) of the last step; waits for it."""
+        n, c, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_int32()
+        self._check(_abi.soma_opt_get_norm(self._h, ctypes.byref(n), ctypes.byref(c), ctypes.byref(f),
+                                           _stream_handle(stream)))
+        return n.value, c.value, bool(f.value)
+
+    def set_timing(self, enable: bool):
+        self._check(_abi.soma_opt_set_timing(self._h, 1 if enable else 0))
+
+    def read_timing(self):
+        """(norm_kernel_ms, update_kernel_ms, steps) summed since the last read."""
+        a, b, s = ctypes.c_double(), ctypes.c_double(), ctypes.c_int64()
+        self._check(_abi.soma_opt_read_timing(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(s)))
+        return a.value, b.value, s.value
+
+    def plan(self) -> dict:
+        p = soma_plan_t()
+        self._check(_abi.soma_opt_get_plan(self._h, ctypes.byref(p)))
+        return {name: getattr(p, name) for name, _ in soma_plan_t._fields_ if name != "reserved"}
+
+    def set_tuning(self, update_chunk: int = 0, norm_chunk: int = 0, ctas_per_sm: int = 0):
+        self._check(_abi.soma_opt_set_tuning(self._h, update_chunk, norm_chunk, ctas_per_sm))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _abi.soma_opt_destroy(self._h)
+            self._h = _abi.soma_opt_t()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

@@ -1,0 +1,121 @@
+"""ctypes declarations of include/soma_opt.h, one Python name per C name.
+
+Loading fails loudly when libsoma_opt.so has not been built: there is no
+fallback implementation of the step anywhere in this package.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+SOMA_OK = 0
+SOMA_ERR_INVALID_ARG = 1
+SOMA_ERR_BAD_GROUP = 2
+SOMA_ERR_DTYPE = 3
+SOMA_ERR_ALIGNMENT = 4
+SOMA_ERR_OOM = 5
+SOMA_ERR_CUDA = 6
+SOMA_ERR_STATE = 7
+SOMA_ERR_LIMIT = 8
+
+SOMA_DTYPE_F32 = 0
+SOMA_DTYPE_BF16 = 1
+SOMA_MAX_GROUPS = 64
+SOMA_ABI_VERSION = 1
+
+soma_status_t = ctypes.c_int32
+soma_opt_t = ctypes.c_void_p
+
+
+class soma_tensor_t(ctypes.Structure):
+    _fields_ = [
+        ("param", ctypes.c_void_p),
+        ("grad", ctypes.c_void_p),
+        ("exp_avg", ctypes.c_void_p),
+        ("exp_avg_sq", ctypes.c_void_p),
+        ("numel", ctypes.c_int64),
+        ("group", ctypes.c_int32),
+        ("grad_dtype", ctypes.c_uint8),
+        ("trainable", ctypes.c_uint8),
+        ("owned", ctypes.c_uint8),
+        ("reserved", ctypes.c_uint8),
+    ]
+
+
+assert ctypes.sizeof(soma_tensor_t) == 48
+
+
+class soma_plan_t(ctypes.Structure):
+    _fields_ = [
+        ("norm_chunks", ctypes.c_int64),
+        ("norm_segments", ctypes.c_int64),
+        ("update_chunks", ctypes.c_int64),
+        ("update_segments", ctypes.c_int64),
+        ("norm_grid", ctypes.c_int32),
+        ("norm_block", ctypes.c_int32),
+        ("update_grid", ctypes.c_int32),
+        ("update_block", ctypes.c_int32),
+        ("trainable_numel", ctypes.c_int64),
+        ("owned_numel", ctypes.c_int64),
+        ("launches_per_step", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+_D = ctypes.c_double
+_DP = ctypes.POINTER(ctypes.c_double)
+_I32 = ctypes.c_int32
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_I64 = ctypes.c_int64
+_I64P = ctypes.POINTER(ctypes.c_int64)
+
+# name -> (restype, argtypes); every function the header declares.
+SIGNATURES = {
+    "soma_opt_create": (soma_status_t, [ctypes.POINTER(soma_opt_t), _I32]),
+    "soma_opt_add_group": (soma_status_t, [soma_opt_t, _D, _D, _D, _D, _D, _I32P]),
+    "soma_opt_set_lr": (soma_status_t, [soma_opt_t, _I32, _D]),
+    "soma_opt_get_group": (soma_status_t, [soma_opt_t, _I32, _DP, _DP, _DP, _DP, _DP]),
+    "soma_opt_set_group": (soma_status_t, [soma_opt_t, _I32, _D, _D, _D, _D, _D]),
+    "soma_opt_get_group_step": (soma_status_t, [soma_opt_t, _I32, _I64P]),
+    "soma_opt_set_group_step": (soma_status_t, [soma_opt_t, _I32, _I64]),
+    "soma_opt_step": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,
+                                      ctypes.c_void_p]),
+    "soma_opt_get_norm": (soma_status_t, [soma_opt_t, _DP, _DP, _I32P, ctypes.c_void_p]),
+    "soma_opt_set_timing": (soma_status_t, [soma_opt_t, _I32]),
+    "soma_opt_read_timing": (soma_status_t, [soma_opt_t, _DP, _DP, _I64P]),
+    "soma_opt_get_plan": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_plan_t)]),
+    "soma_opt_set_tuning": (soma_status_t, [soma_opt_t, _I32, _I32, _I32]),
+    "soma_status_string": (ctypes.c_char_p, [soma_status_t]),
+    "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),
+    "soma_abi_version": (_I32, []),
+    "soma_opt_destroy": (None, [soma_opt_t]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libsoma_opt.so (built by tensor_grad_clip_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m tensor_grad_clip_gb300.build` "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+        globals()[name] = fn
+    if lib.soma_abi_version() != SOMA_ABI_VERSION:
+        raise RuntimeError(f"{path}: ABI version {lib.soma_abi_version()}, expected {SOMA_ABI_VERSION}")
+    _lib = lib
+    return lib

@@ -1,0 +1,295 @@
+// The two kernels of one optimizer step (sm_103a).
+//
+//  norm_kernel   -- owned square-sum.  Every CTA walks chunks of the norm
+//                   table, sums g^2 of its chunk in fp32 (per-thread
+//                   accumulators, then a fixed-shape warp/block tree) and
+//                   stores the chunk's sum at partials[chunk].  The last CTA
+//                   to arrive (atomic ticket; nobody waits) adds the partials
+//                   in fp64 in a fixed order, so the norm is the same bits
+//                   on every run whatever the CTA schedule, then derives
+//                   norm = sqrt(S)/d and c = min(1, max_norm/(norm + 1e-6)).
+//                   This is the "statistics needed for one global clipping
+//                   decision" of the SomaSpeed optimizer paragraphs, with
+//                   ownership resolved by the host (only owned segments are
+//                   in this table).
+//
+//  update_kernel -- the fused normalize + clip + AdamW pass.  It reads the
+//                   scale c/d that the norm kernel left in device memory (no
+//                   host round trip) and streams every trainable element once:
+//                   g (2 or 4 B) and p, m, v (4 B each) in, p, m, v out.
+//                   Gradients are never written.
+//
+// Both kernels are HBM-bound streams (about 0.5 flop per byte); they use
+// 16-byte vector accesses and no tensor cores.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "soma_kernels.h"
+
+namespace soma {
+namespace {
+
+// bf16 is the upper half of a binary32: widening is a shift / mask.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_one(uint16_t w) { return __uint_as_float((uint32_t)w << 16); }
+
+// Copy the chunk's segment descriptors into shared memory (3 x 16 B each).
+__device__ __forceinline__ int stage_segments(const Table& t, int chunk, Seg* sm) {
+    const int b = __ldg(t.chunk_begin + chunk);
+    const int n = __ldg(t.chunk_begin + chunk + 1) - b;
+    const uint4* src = reinterpret_cast<const uint4*>(t.segs + b);
+    uint4* dst = reinterpret_cast<uint4*>(sm);
+    for (int i = threadIdx.x; i < 3 * n; i += blockDim.x) dst[i] = __ldg(src + i);
+    __syncthreads();
+    return n;
+}
+
+template <int BLOCK>
+__device__ __forceinline__ float block_sum(float x, float* scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) scratch[w] = x;
+    __syncthreads();
+    float r = 0.f;
+    if (w == 0) {
+        r = (l < BLOCK / 32) ? scratch[l] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    }
+    return r;  // valid in thread 0
+}
+
+template <int BLOCK>
+__device__ __forceinline__ double block_sum64(double x, double* scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) scratch[w] = x;
+    __syncthreads();
+    double r = 0.0;
+    if (w == 0) {
+        r = (l < BLOCK / 32) ? scratch[l] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    }
+    return r;
+}
+
+// ---- square-sum of one segment, accumulated into acc[0..1] --------------
+
+__device__ __forceinline__ void sumsq_bf16(const Seg& s, float& a0, float& a1) {
+    const uint16_t* g = static_cast<const uint16_t*>(s.g);
+    for (int j = threadIdx.x; j < s.head; j += blockDim.x) {
+        float x = bf16_one(__ldg(g + j));
+        a0 = fmaf(x, x, a0);
+    }
+    const uint4* gv = reinterpret_cast<const uint4*>(g + s.head);
+    for (int i = threadIdx.x; i < s.nvec; i += blockDim.x) {
+        uint4 w = __ldg(gv + i);
+        float x;
+        x = bf16_lo(w.x); a0 = fmaf(x, x, a0);
+        x = bf16_hi(w.x); a1 = fmaf(x, x, a1);
+        x = bf16_lo(w.y); a0 = fmaf(x, x, a0);
+        x = bf16_hi(w.y); a1 = fmaf(x, x, a1);
+        x = bf16_lo(w.z); a0 = fmaf(x, x, a0);
+        x = bf16_hi(w.z); a1 = fmaf(x, x, a1);
+        x = bf16_lo(w.w); a0 = fmaf(x, x, a0);
+        x = bf16_hi(w.w); a1 = fmaf(x, x, a1);
+    }
+    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
+        float x = bf16_one(__ldg(g + j));
+        a1 = fmaf(x, x, a1);
+    }
+}
+
+__device__ __forceinline__ void sumsq_f32(const Seg& s, float& a0, float& a1) {
+    const float* g = static_cast<const float*>(s.g);
+    for (int j = threadIdx.x; j < s.head; j += blockDim.x) {
+        float x = __ldg(g + j);
+        a0 = fmaf(x, x, a0);
+    }
+    const float4* gv = reinterpret_cast<const float4*>(g + s.head);
+    for (int i = threadIdx.x; i < s.nvec; i += blockDim.x) {
+        float4 u = __ldg(gv + 2 * i);
+        float4 w = __ldg(gv + 2 * i + 1);
+        a0 = fmaf(u.x, u.x, a0); a1 = fmaf(u.y, u.y, a1);
+        a0 = fmaf(u.z, u.z, a0); a1 = fmaf(u.w, u.w, a1);
+        a0 = fmaf(w.x, w.x, a0); a1 = fmaf(w.y, w.y, a1);
+        a0 = fmaf(w.z, w.z, a0); a1 = fmaf(w.w, w.w, a1);
+    }
+    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
+        float x = __ldg(g + j);
+        a1 = fmaf(x, x, a1);
+    }
+}
+
+__global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant__ NormArgs a) {
+    __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
+    __shared__ float wsum[kNormBlock / 32];
+    __shared__ double wsum64[kNormBlock / 32];
+    __shared__ int last;
+
+    for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
+        const int ns = stage_segments(a.t, c, segs);
+        float a0 = 0.f, a1 = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            if (segs[s].gdtype == kBF16) sumsq_bf16(segs[s], a0, a1);
+            else sumsq_f32(segs[s], a0, a1);
+        }
+        const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
+        if (threadIdx.x == 0) a.partials[c] = (double)bs;
+        __syncthreads();  // segs and wsum are reused by the next chunk
+    }
+
+    // Arrival: the last CTA to finish reduces all partials.  No CTA waits.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned t = atomicAdd(&a.res->ticket, 1u);
+        last = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+
+    double s = 0.0;
+    for (int i = threadIdx.x; i < a.t.nchunks; i += blockDim.x) s += __ldcg(a.partials + i);
+    s = block_sum64<kNormBlock>(s, wsum64);
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(s) / a.divisor;
+        const double q = a.max_norm / (norm + 1e-6);
+        const double coef = (q < 1.0 || q != q) ? q : 1.0;  // NaN propagates
+        a.res->sumsq = s;
+        a.res->norm = norm;
+        a.res->coef = coef;
+        a.res->scale = (float)(coef / a.divisor);
+        a.res->nonfinite = isfinite(norm) ? 0u : 1u;
+        a.res->ticket = 0u;
+    }
+}
+
+// ---- fused update --------------------------------------------------------
+
+__device__ __forceinline__ void adamw(float& p, float& m, float& v, float g, const GroupHp& h) {
+    p *= h.decay;
+    m = fmaf(h.beta1, m, h.one_minus_beta1 * g);
+    v = fmaf(h.beta2, v, h.one_minus_beta2 * (g * g));
+    const float denom = fmaf(sqrtf(v), h.inv_sqrt_bc2, h.eps);
+    p = fmaf(-h.step_size, m / denom, p);
+}
+
+__device__ __forceinline__ float grad_one(const Seg& s, int j) {
+    return s.gdtype == kBF16 ? bf16_one(__ldcs(static_cast<const unsigned short*>(s.g) + j))
+                             : __ldcs(static_cast<const float*>(s.g) + j);
+}
+
+__device__ __forceinline__ void update_one(const Seg& s, int j, const GroupHp& h, float scale) {
+    float p = __ldcs(s.p + j), m = __ldcs(s.m + j), v = __ldcs(s.v + j);
+    adamw(p, m, v, grad_one(s, j) * scale, h);
+    __stcs(s.p + j, p);
+    __stcs(s.m + j, m);
+    __stcs(s.v + j, v);
+}
+
+struct Lane8 {
+    float g[8];
+    float4 p0, p1, m0, m1, v0, v1;
+};
+
+template <int DT>
+__device__ __forceinline__ void load8(const Seg& s, int i, Lane8& x) {
+    const float4* p = reinterpret_cast<const float4*>(s.p + s.head) + 2 * i;
+    const float4* m = reinterpret_cast<const float4*>(s.m + s.head) + 2 * i;
+    const float4* v = reinterpret_cast<const float4*>(s.v + s.head) + 2 * i;
+    if (DT == kBF16) {
+        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(
+                                   static_cast<const uint16_t*>(s.g) + s.head) + i);
+        x.g[0] = bf16_lo(w.x); x.g[1] = bf16_hi(w.x);
+        x.g[2] = bf16_lo(w.y); x.g[3] = bf16_hi(w.y);
+        x.g[4] = bf16_lo(w.z); x.g[5] = bf16_hi(w.z);
+        x.g[6] = bf16_lo(w.w); x.g[7] = bf16_hi(w.w);
+    } else {
+        const float4* g = reinterpret_cast<const float4*>(static_cast<const float*>(s.g) + s.head) + 2 * i;
+        const float4 u = __ldcs(g), w = __ldcs(g + 1);
+        x.g[0] = u.x; x.g[1] = u.y; x.g[2] = u.z; x.g[3] = u.w;
+        x.g[4] = w.x; x.g[5] = w.y; x.g[6] = w.z; x.g[7] = w.w;
+    }
+    x.p0 = __ldcs(p); x.p1 = __ldcs(p + 1);
+    x.m0 = __ldcs(m); x.m1 = __ldcs(m + 1);
+    x.v0 = __ldcs(v); x.v1 = __ldcs(v + 1);
+}
+
+__device__ __forceinline__ void compute8(Lane8& x, const GroupHp& h, float scale) {
+    adamw(x.p0.x, x.m0.x, x.v0.x, x.g[0] * scale, h);
+    adamw(x.p0.y, x.m0.y, x.v0.y, x.g[1] * scale, h);
+    adamw(x.p0.z, x.m0.z, x.v0.z, x.g[2] * scale, h);
+    adamw(x.p0.w, x.m0.w, x.v0.w, x.g[3] * scale, h);
+    adamw(x.p1.x, x.m1.x, x.v1.x, x.g[4] * scale, h);
+    adamw(x.p1.y, x.m1.y, x.v1.y, x.g[5] * scale, h);
+    adamw(x.p1.z, x.m1.z, x.v1.z, x.g[6] * scale, h);
+    adamw(x.p1.w, x.m1.w, x.v1.w, x.g[7] * scale, h);
+}
+
+__device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
+    float4* p = reinterpret_cast<float4*>(s.p + s.head) + 2 * i;
+    float4* m = reinterpret_cast<float4*>(s.m + s.head) + 2 * i;
+    float4* v = reinterpret_cast<float4*>(s.v + s.head) + 2 * i;
+    __stcs(p, x.p0); __stcs(p + 1, x.p1);
+    __stcs(m, x.m0); __stcs(m + 1, x.m1);
+    __stcs(v, x.v0); __stcs(v + 1, x.v1);
+}
+
+template <int DT>
+__device__ __forceinline__ void update_body(const Seg& s, const GroupHp& h, float scale) {
+    const int n = s.nvec;
+    const int stride = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + stride < n; i += 2 * stride) {  // two vectors in flight per thread
+        Lane8 x0, x1;
+        load8<DT>(s, i, x0);
+        load8<DT>(s, i + stride, x1);
+        compute8(x0, h, scale);
+        compute8(x1, h, scale);
+        store8(s, i, x0);
+        store8(s, i + stride, x1);
+    }
+    if (i < n) {
+        Lane8 x0;
+        load8<DT>(s, i, x0);
+        compute8(x0, h, scale);
+        store8(s, i, x0);
+    }
+}
+
+__global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_constant__ UpdateArgs a) {
+    __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
+    const float scale = __ldcg(&a.res->scale);
+    for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
+        const int ns = stage_segments(a.t, c, segs);
+        for (int k = 0; k < ns; ++k) {
+            const Seg& s = segs[k];
+            const GroupHp& h = a.groups[s.group];
+            for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one(s, j, h, scale);
+            if (s.gdtype == kBF16) update_body<kBF16>(s, h, scale);
+            else update_body<kF32>(s, h, scale);
+            for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x)
+                update_one(s, j, h, scale);
+        }
+        __syncthreads();  // segs is restaged for the next chunk
+    }
+}
+
+}  // namespace
+
+int launch_norm(const NormArgs& a, int grid, void* stream) {
+    norm_kernel<<<grid, kNormBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_update(const UpdateArgs& a, int grid, void* stream) {
+    update_kernel<<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace soma

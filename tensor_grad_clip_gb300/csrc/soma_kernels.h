@@ -1,0 +1,98 @@
+// Device-side data layout shared by the host library and the kernels.
+//
+// A step streams two tables, both built on the host from the caller's list
+// and uploaded once per distinct list:
+//
+//   * the update table covers every trainable element; the norm table covers
+//     the trainable, owned elements only (non-owned entries never reach the
+//     square-sum kernel, so that kernel has no ownership branch);
+//   * a table is a sequence of segments -- a contiguous element range of one
+//     tensor -- grouped into chunks of about the same number of elements.
+//     One CTA processes one chunk at a time.  Small tensors share a chunk,
+//     large tensors are cut into several; so one launch covers the whole
+//     list however many tensors it has (the "many small tensors" case of the
+//     SomaSpeed optimizer paragraphs).
+//
+// Vector body: inside a segment, elements [head, head + 8*nvec) are processed
+// eight at a time with 16-byte accesses; the host picks `head` so that every
+// buffer is 16-byte aligned there, and cuts tensors only at such points.  The
+// few elements before and after run one at a time.  A tensor whose buffers
+// cannot all be aligned at one element is processed one element at a time.
+#pragma once
+
+#include <cstdint>
+
+namespace soma {
+
+constexpr int kVec = 8;                 // elements per vector step
+constexpr int kMaxSegsPerChunk = 64;    // bounds the shared-memory segment cache
+constexpr int kMaxGroups = 64;
+
+enum : int32_t { kF32 = 0, kBF16 = 1 };
+
+struct Seg {                // 48 bytes
+    float* p;               // already offset to the segment's first element
+    const void* g;
+    float* m;
+    float* v;
+    int32_t len;            // elements in the segment
+    int32_t head;           // scalar elements before the vector body
+    int32_t nvec;           // 8-element vectors in the body
+    uint16_t group;
+    uint8_t gdtype;
+    uint8_t pad;
+};
+static_assert(sizeof(Seg) == 48, "Seg layout");
+
+// Per-group constants of one step, derived on the host in fp64 and rounded
+// once to fp32.
+struct GroupHp {
+    float decay;            // 1 - lr * weight_decay
+    float beta1, one_minus_beta1;
+    float beta2, one_minus_beta2;
+    float step_size;        // lr / (1 - beta1^t)
+    float inv_sqrt_bc2;     // 1 / sqrt(1 - beta2^t)
+    float eps;
+};
+
+// Written by the square-sum kernel's last CTA, read by the update kernel and
+// by soma_opt_get_norm.
+struct Result {
+    double sumsq;           // sum of g^2 over owned elements (stored gradients)
+    double norm;            // sqrt(sumsq) / d
+    double coef;            // min(1, max_norm / (norm + 1e-6))
+    float scale;            // coef / d in fp32: the update multiplies g by this
+    uint32_t nonfinite;     // 1 when norm is not finite
+    uint32_t ticket;        // CTA arrival counter; the last CTA resets it to 0
+    uint32_t pad[3];
+};
+static_assert(sizeof(Result) == 48, "Result layout");
+
+struct Table {
+    const Seg* segs;
+    const int32_t* chunk_begin;  // nchunks + 1 entries
+    int32_t nchunks;
+};
+
+struct NormArgs {
+    Table t;
+    double* partials;       // one per chunk
+    Result* res;
+    double divisor;
+    double max_norm;
+};
+
+struct UpdateArgs {
+    Table t;
+    const Result* res;
+    GroupHp groups[kMaxGroups];
+};
+
+constexpr int kNormBlock = 512;
+constexpr int kUpdateBlock = 256;
+
+// Launch wrappers (kernels.cu).  Return the cudaError_t of the launch as int.
+int launch_norm(const NormArgs& a, int grid, void* stream);
+int launch_update(const UpdateArgs& a, int grid, void* stream);
+
+}  // namespace soma

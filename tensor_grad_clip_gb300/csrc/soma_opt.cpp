@@ -1,0 +1,657 @@
+// Host side of the C ABI declared in include/soma_opt.h.
+//
+// soma_opt_step: check every argument (nothing changes on failure) -> if the
+// list differs from the previous call's, rebuild the norm and update tables
+// on the host and upload them -> derive each group's per-step constants in
+// fp64 -> enqueue the square-sum kernel, then the update kernel, on the
+// caller's stream.  The clip coefficient never leaves the device.
+#include "soma_opt.h"
+
+#include <cuda_runtime.h>
+
+#include <array>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include "soma_kernels.h"
+
+namespace {
+
+constexpr int32_t kDefaultUpdateChunk = 16384;
+constexpr int32_t kDefaultNormChunk = 32768;
+constexpr size_t kTimingRing = 1024;
+
+struct Group {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+};
+
+thread_local std::string g_create_error;
+std::mutex g_live_mu;
+std::unordered_set<const void*> g_live;
+
+bool is_live(const void* h) {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    return h != nullptr && g_live.count(h) != 0;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct soma_opt {
+    int32_t device = 0;
+    std::vector<Group> groups;
+    std::string err;
+
+    int32_t update_chunk = kDefaultUpdateChunk;
+    int32_t norm_chunk = kDefaultNormChunk;
+    int32_t ctas_per_sm = 0;
+
+    // device state, created on first use
+    bool dev_ready = false;
+    int sm_count = 0;
+    soma::Result* d_res = nullptr;
+    soma::Result* h_res = nullptr;  // pinned
+    double* d_partials = nullptr;
+    size_t partials_cap = 0;        // elements
+    char* d_tables = nullptr;
+    size_t tables_cap = 0;          // bytes
+    char* h_staging = nullptr;      // pinned
+    size_t staging_cap = 0;
+    cudaEvent_t done = nullptr;     // recorded after each step's last kernel
+    bool have_done = false;
+    void* last_stream = nullptr;
+
+    // the list the device tables describe
+    std::vector<soma_tensor_t> cached;
+    bool cache_valid = false;
+    soma::Table norm_tab{}, upd_tab{};
+    std::vector<uint8_t> group_present;
+    int norm_grid = 1, upd_grid = 0;
+    soma_plan_t plan{};
+
+    // kernel timing
+    bool timing = false;
+    std::vector<std::array<cudaEvent_t, 3>> tev;
+    size_t tev_used = 0;
+    double acc_norm_ms = 0.0, acc_upd_ms = 0.0;
+    int64_t acc_steps = 0;
+
+    soma_status_t fail(soma_status_t st, const char* fmt, ...) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        err = std::string(soma_status_string(st)) + ": " + buf;
+        return st;
+    }
+    soma_status_t cuda_fail(cudaError_t e, const char* what) {
+        cudaGetLastError();  // clear a non-sticky error so later calls start clean
+        return fail(e == cudaErrorMemoryAllocation ? SOMA_ERR_OOM : SOMA_ERR_CUDA, "%s: %s (%d)",
+                    what, cudaGetErrorString(e), (int)e);
+    }
+};
+
+namespace {
+
+// Makes `dev` current for the scope and restores the caller's device.
+struct DeviceGuard {
+    int prev = -1;
+    cudaError_t status = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        status = cudaGetDevice(&prev);
+        if (status == cudaSuccess && prev != dev) status = cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool is_finite(double x) { return std::isfinite(x); }
+
+soma_status_t check_group_hp(soma_opt* o, double lr, double b1, double b2, double eps, double wd) {
+    if (!is_finite(lr) || lr < 0) return o->fail(SOMA_ERR_INVALID_ARG, "lr must be finite and >= 0 (got %g)", lr);
+    if (!is_finite(b1) || b1 < 0 || b1 >= 1) return o->fail(SOMA_ERR_INVALID_ARG, "beta1 must be in [0, 1) (got %g)", b1);
+    if (!is_finite(b2) || b2 < 0 || b2 >= 1) return o->fail(SOMA_ERR_INVALID_ARG, "beta2 must be in [0, 1) (got %g)", b2);
+    if (!is_finite(eps) || eps <= 0) return o->fail(SOMA_ERR_INVALID_ARG, "eps must be finite and > 0 (got %g)", eps);
+    if (!is_finite(wd) || wd < 0) return o->fail(SOMA_ERR_INVALID_ARG, "weight_decay must be finite and >= 0 (got %g)", wd);
+    return SOMA_OK;
+}
+
+soma_status_t validate_entry(soma_opt* o, const soma_tensor_t& t, int64_t k) {
+    if (t.reserved != 0) return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld].reserved must be 0", (long long)k);
+    if (t.trainable > 1 || t.owned > 1)
+        return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld]: trainable and owned must be 0 or 1", (long long)k);
+    if (t.numel < 0) return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld].numel < 0", (long long)k);
+    if (!t.trainable) return SOMA_OK;
+    if (t.group < 0 || t.group >= (int32_t)o->groups.size())
+        return o->fail(SOMA_ERR_BAD_GROUP, "list[%lld].group = %d, have %zu groups", (long long)k, t.group,
+                       o->groups.size());
+    if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16)
+        return o->fail(SOMA_ERR_DTYPE, "list[%lld].grad_dtype = %d", (long long)k, (int)t.grad_dtype);
+    if (t.numel == 0) return SOMA_OK;
+    if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq)
+        return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld]: null buffer in a trainable entry", (long long)k);
+    const uintptr_t ge = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
+    if ((uintptr_t)t.param % 4 || (uintptr_t)t.exp_avg % 4 || (uintptr_t)t.exp_avg_sq % 4 ||
+        (uintptr_t)t.grad % ge)
+        return o->fail(SOMA_ERR_ALIGNMENT, "list[%lld]: a buffer is not aligned to its element size",
+                       (long long)k);
+    return SOMA_OK;
+}
+
+// Smallest h in [0, 8) at which every listed buffer is 16-byte aligned, or -1.
+int vector_head(const uintptr_t* addr, const int* esize, int n) {
+    for (int h = 0; h < soma::kVec; ++h) {
+        bool ok = true;
+        for (int k = 0; k < n && ok; ++k) ok = (addr[k] + (uintptr_t)h * esize[k]) % 16 == 0;
+        if (ok) return h;
+    }
+    return -1;
+}
+
+// Cuts tensors into segments and groups segments into chunks of about
+// `chunk` elements (at most kMaxSegsPerChunk segments each).
+struct TableBuilder {
+    int64_t chunk;
+    std::vector<soma::Seg> segs;
+    std::vector<int32_t> begin{0};
+    int64_t cur_elems = 0;
+    int cur_segs = 0;
+
+    explicit TableBuilder(int64_t c) : chunk(c) {}
+
+    void close() {
+        if (cur_segs == 0) return;
+        begin.push_back((int32_t)segs.size());
+        cur_elems = 0;
+        cur_segs = 0;
+    }
+
+    // h: vector head of the tensor, -1 = process every element singly.
+    void add(const soma_tensor_t& t, int h, bool with_state) {
+        const int64_t n = t.numel;
+        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
+        int64_t off = 0;
+        while (off < n) {
+            if (cur_segs == soma::kMaxSegsPerChunk || cur_elems >= chunk) close();
+            int64_t cut = off + std::min(n - off, chunk - cur_elems);
+            if (h >= 0 && cut < n && cut > h) {  // cut on the vector grid
+                cut = h + (cut - h + soma::kVec - 1) / soma::kVec * soma::kVec;
+                if (cut > n) cut = n;
+            }
+            const int64_t len = cut - off;
+            soma::Seg s{};
+            s.p = with_state ? t.param + off : nullptr;
+            s.m = with_state ? t.exp_avg + off : nullptr;
+            s.v = with_state ? t.exp_avg_sq + off : nullptr;
+            s.g = static_cast<const char*>(t.grad) + off * gsz;
+            s.len = (int32_t)len;
+            if (h < 0) {
+                s.head = (int32_t)len;
+                s.nvec = 0;
+            } else {
+                s.head = off < h ? (int32_t)std::min<int64_t>(h - off, len) : 0;
+                s.nvec = (int32_t)((len - s.head) / soma::kVec);
+            }
+            s.group = (uint16_t)t.group;
+            s.gdtype = t.grad_dtype;
+            segs.push_back(s);
+            cur_elems += len;
+            ++cur_segs;
+            off = cut;
+        }
+    }
+    int32_t nchunks() const { return (int32_t)begin.size() - 1; }
+};
+
+soma_status_t ensure_device(soma_opt* o) {
+    if (o->dev_ready) return SOMA_OK;
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&o->sm_count, cudaDevAttrMultiProcessorCount, o->device)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaMalloc(&o->d_res, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMalloc(result)");
+    if ((e = cudaMemset(o->d_res, 0, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMemset(result)");
+    if ((e = cudaMallocHost(&o->h_res, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMallocHost");
+    if ((e = cudaEventCreateWithFlags(&o->done, cudaEventDisableTiming)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventCreate");
+    o->dev_ready = true;
+    return SOMA_OK;
+}
+
+// Waits until no kernel of a previous step can still read the tables,
+// partials or staging buffer.
+soma_status_t wait_idle(soma_opt* o) {
+    if (!o->have_done) return SOMA_OK;
+    cudaError_t e = cudaEventSynchronize(o->done);
+    return e == cudaSuccess ? SOMA_OK : o->cuda_fail(e, "cudaEventSynchronize");
+}
+
+soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* stream) {
+    TableBuilder upd(o->update_chunk), nrm(o->norm_chunk);
+    std::vector<uint8_t> present(o->groups.size(), 0);
+    int64_t trainable = 0, owned = 0;
+    for (int64_t k = 0; k < n; ++k) {
+        const soma_tensor_t& t = list[k];
+        if (!t.trainable) continue;
+        present[t.group] = 1;
+        if (t.numel == 0) continue;
+        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
+        const uintptr_t a4[4] = {(uintptr_t)t.grad, (uintptr_t)t.param, (uintptr_t)t.exp_avg,
+                                 (uintptr_t)t.exp_avg_sq};
+        const int e4[4] = {gsz, 4, 4, 4};
+        upd.add(t, vector_head(a4, e4, 4), true);
+        trainable += t.numel;
+        if (t.owned) {
+            nrm.add(t, vector_head(a4, e4, 1), false);
+            owned += t.numel;
+        }
+    }
+    upd.close();
+    nrm.close();
+
+    // layout: [update segs][norm segs][update chunk_begin][norm chunk_begin]
+    const size_t o_us = 0;
+    const size_t o_ns = align_up(o_us + upd.segs.size() * sizeof(soma::Seg), 256);
+    const size_t o_ub = align_up(o_ns + nrm.segs.size() * sizeof(soma::Seg), 256);
+    const size_t o_nb = align_up(o_ub + upd.begin.size() * sizeof(int32_t), 256);
+    const size_t bytes = align_up(o_nb + nrm.begin.size() * sizeof(int32_t), 256);
+    const size_t nparts = std::max<size_t>(1, (size_t)nrm.nchunks());
+
+    soma_status_t st = wait_idle(o);
+    if (st != SOMA_OK) return st;
+    cudaError_t e;
+    if (bytes > o->staging_cap) {
+        if (o->h_staging) cudaFreeHost(o->h_staging);
+        o->h_staging = nullptr;
+        o->staging_cap = 0;
+        if ((e = cudaMallocHost(&o->h_staging, bytes)) != cudaSuccess) return o->cuda_fail(e, "cudaMallocHost(tables)");
+        o->staging_cap = bytes;
+    }
+    if (bytes > o->tables_cap) {
+        if (o->d_tables) cudaFree(o->d_tables);
+        o->d_tables = nullptr;
+        o->tables_cap = 0;
+        if ((e = cudaMalloc(&o->d_tables, bytes)) != cudaSuccess) return o->cuda_fail(e, "cudaMalloc(tables)");
+        o->tables_cap = bytes;
+    }
+    if (nparts > o->partials_cap) {
+        if (o->d_partials) cudaFree(o->d_partials);
+        o->d_partials = nullptr;
+        o->partials_cap = 0;
+        if ((e = cudaMalloc(&o->d_partials, nparts * sizeof(double))) != cudaSuccess)
+            return o->cuda_fail(e, "cudaMalloc(partials)");
+        o->partials_cap = nparts;
+    }
+    char* h = o->h_staging;
+    std::memcpy(h + o_us, upd.segs.data(), upd.segs.size() * sizeof(soma::Seg));
+    std::memcpy(h + o_ns, nrm.segs.data(), nrm.segs.size() * sizeof(soma::Seg));
+    std::memcpy(h + o_ub, upd.begin.data(), upd.begin.size() * sizeof(int32_t));
+    std::memcpy(h + o_nb, nrm.begin.data(), nrm.begin.size() * sizeof(int32_t));
+    if ((e = cudaMemcpyAsync(o->d_tables, h, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMemcpyAsync(tables)");
+
+    char* d = o->d_tables;
+    o->upd_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_us),
+                             reinterpret_cast<const int32_t*>(d + o_ub), upd.nchunks()};
+    o->norm_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_ns),
+                              reinterpret_cast<const int32_t*>(d + o_nb), nrm.nchunks()};
+    const int64_t cap = o->ctas_per_sm > 0 ? (int64_t)o->sm_count * o->ctas_per_sm : INT32_MAX;
+    o->upd_grid = (int)std::min<int64_t>(upd.nchunks(), cap);
+    o->norm_grid = (int)std::max<int64_t>(1, std::min<int64_t>(nrm.nchunks(), cap));
+    o->group_present = present;
+    o->cached.assign(list, list + n);
+    o->cache_valid = true;
+
+    soma_plan_t& p = o->plan;
+    p.norm_chunks = nrm.nchunks();
+    p.norm_segments = (int64_t)nrm.segs.size();
+    p.update_chunks = upd.nchunks();
+    p.update_segments = (int64_t)upd.segs.size();
+    p.norm_grid = o->norm_grid;
+    p.norm_block = soma::kNormBlock;
+    p.update_grid = o->upd_grid;
+    p.update_block = soma::kUpdateBlock;
+    p.trainable_numel = trainable;
+    p.owned_numel = owned;
+    p.launches_per_step = 1 + (o->upd_grid > 0 ? 1 : 0);
+    return SOMA_OK;
+}
+
+soma_status_t timing_flush(soma_opt* o) {
+    for (size_t i = 0; i < o->tev_used; ++i) {
+        cudaError_t e = cudaEventSynchronize(o->tev[i][2]);
+        if (e != cudaSuccess) return o->cuda_fail(e, "cudaEventSynchronize(timing)");
+        float a = 0.f, b = 0.f;
+        if ((e = cudaEventElapsedTime(&a, o->tev[i][0], o->tev[i][1])) != cudaSuccess ||
+            (e = cudaEventElapsedTime(&b, o->tev[i][1], o->tev[i][2])) != cudaSuccess)
+            return o->cuda_fail(e, "cudaEventElapsedTime");
+        o->acc_norm_ms += a;
+        o->acc_upd_ms += b;
+        o->acc_steps += 1;
+    }
+    o->tev_used = 0;
+    return SOMA_OK;
+}
+
+soma_opt* live_handle(soma_opt_t h) { return is_live(h) ? h : nullptr; }
+
+}  // namespace
+
+extern "C" {
+
+const char* soma_status_string(soma_status_t s) {
+    switch (s) {
+        case SOMA_OK: return "ok";
+        case SOMA_ERR_INVALID_ARG: return "invalid argument";
+        case SOMA_ERR_BAD_GROUP: return "unknown parameter group";
+        case SOMA_ERR_DTYPE: return "unsupported gradient dtype";
+        case SOMA_ERR_ALIGNMENT: return "misaligned buffer";
+        case SOMA_ERR_OOM: return "out of memory";
+        case SOMA_ERR_CUDA: return "CUDA error";
+        case SOMA_ERR_STATE: return "invalid handle or state";
+        case SOMA_ERR_LIMIT: return "limit exceeded";
+        default: return "unknown status";
+    }
+}
+
+int32_t soma_abi_version(void) { return SOMA_ABI_VERSION; }
+
+soma_status_t soma_opt_create(soma_opt_t* out, int32_t device) {
+    if (!out) {
+        g_create_error = "invalid argument: out is NULL";
+        return SOMA_ERR_INVALID_ARG;
+    }
+    *out = nullptr;
+    if (device < 0) {
+        g_create_error = "invalid argument: device < 0";
+        return SOMA_ERR_INVALID_ARG;
+    }
+    soma_opt* o = new (std::nothrow) soma_opt();
+    if (!o) {
+        g_create_error = "out of memory: handle";
+        return SOMA_ERR_OOM;
+    }
+    o->device = device;
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        g_live.insert(o);
+    }
+    *out = o;
+    return SOMA_OK;
+}
+
+const char* soma_opt_last_error(soma_opt_t h) {
+    if (h == nullptr) return g_create_error.c_str();
+    soma_opt* o = live_handle(h);
+    return o ? o->err.c_str() : "invalid handle";
+}
+
+soma_status_t soma_opt_add_group(soma_opt_t h, double lr, double beta1, double beta2, double eps,
+                                 double weight_decay, int32_t* group_id) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!group_id) return o->fail(SOMA_ERR_INVALID_ARG, "group_id is NULL");
+    soma_status_t st = check_group_hp(o, lr, beta1, beta2, eps, weight_decay);
+    if (st != SOMA_OK) return st;
+    if ((int)o->groups.size() >= SOMA_MAX_GROUPS)
+        return o->fail(SOMA_ERR_LIMIT, "at most %d parameter groups", SOMA_MAX_GROUPS);
+    o->groups.push_back(Group{lr, beta1, beta2, eps, weight_decay, 0});
+    *group_id = (int32_t)o->groups.size() - 1;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_set_lr(soma_opt_t h, int32_t group, double lr) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    if (!is_finite(lr) || lr < 0) return o->fail(SOMA_ERR_INVALID_ARG, "lr must be finite and >= 0 (got %g)", lr);
+    o->groups[group].lr = lr;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_get_group(soma_opt_t h, int32_t group, double* lr, double* beta1, double* beta2,
+                                 double* eps, double* weight_decay) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    const Group& g = o->groups[group];
+    if (lr) *lr = g.lr;
+    if (beta1) *beta1 = g.beta1;
+    if (beta2) *beta2 = g.beta2;
+    if (eps) *eps = g.eps;
+    if (weight_decay) *weight_decay = g.weight_decay;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_set_group(soma_opt_t h, int32_t group, double lr, double beta1, double beta2,
+                                 double eps, double weight_decay) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    soma_status_t st = check_group_hp(o, lr, beta1, beta2, eps, weight_decay);
+    if (st != SOMA_OK) return st;
+    Group& g = o->groups[group];
+    g.lr = lr;
+    g.beta1 = beta1;
+    g.beta2 = beta2;
+    g.eps = eps;
+    g.weight_decay = weight_decay;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_get_group_step(soma_opt_t h, int32_t group, int64_t* t) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    if (!t) return o->fail(SOMA_ERR_INVALID_ARG, "t is NULL");
+    *t = o->groups[group].step;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_set_group_step(soma_opt_t h, int32_t group, int64_t t) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    if (t < 0) return o->fail(SOMA_ERR_INVALID_ARG, "step count must be >= 0");
+    o->groups[group].step = t;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t norm_chunk, int32_t ctas_per_sm) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    auto ok_chunk = [](int32_t c) { return c == 0 || (c >= 64 && c <= (1 << 26)); };
+    if (!ok_chunk(update_chunk) || !ok_chunk(norm_chunk))
+        return o->fail(SOMA_ERR_INVALID_ARG, "chunk sizes must be 0 or in [64, 2^26]");
+    if (ctas_per_sm < 0 || ctas_per_sm > 64) return o->fail(SOMA_ERR_INVALID_ARG, "ctas_per_sm must be in [0, 64]");
+    o->update_chunk = update_chunk ? update_chunk / 64 * 64 : kDefaultUpdateChunk;
+    o->norm_chunk = norm_chunk ? norm_chunk / 64 * 64 : kDefaultNormChunk;
+    o->ctas_per_sm = ctas_per_sm;
+    o->cache_valid = false;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,
+                            double max_norm, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (n < 0) return o->fail(SOMA_ERR_INVALID_ARG, "n < 0");
+    if (n > 0 && !list) return o->fail(SOMA_ERR_INVALID_ARG, "list is NULL with n > 0");
+    if (!is_finite(grad_divisor) || grad_divisor <= 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "grad_divisor must be finite and > 0 (got %g)", grad_divisor);
+    if (!is_finite(max_norm) || max_norm <= 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "max_norm must be finite and > 0 (got %g)", max_norm);
+
+    // An unchanged list was validated when it was cached (groups are never removed).
+    const bool same = o->cache_valid && (int64_t)o->cached.size() == n &&
+                      (n == 0 || std::memcmp(o->cached.data(), list, (size_t)n * sizeof(soma_tensor_t)) == 0);
+    if (!same) {
+        for (int64_t k = 0; k < n; ++k) {
+            soma_status_t st = validate_entry(o, list[k], k);
+            if (st != SOMA_OK) return st;
+        }
+    }
+
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    soma_status_t st = ensure_device(o);
+    if (st != SOMA_OK) return st;
+    cudaError_t e;
+    if (o->have_done && o->last_stream != stream) {
+        // order this step after the previous one, whatever stream that ran on
+        if ((e = cudaStreamWaitEvent((cudaStream_t)stream, o->done, 0)) != cudaSuccess)
+            return o->cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    if (!same) {
+        o->cache_valid = false;
+        if ((st = rebuild(o, list, n, stream)) != SOMA_OK) return st;
+    }
+
+    // Per-group constants for this step (fp64 on the host, rounded once).
+    soma::UpdateArgs ua{};
+    ua.t = o->upd_tab;
+    ua.res = o->d_res;
+    std::vector<int64_t> next(o->groups.size());
+    for (size_t q = 0; q < o->groups.size(); ++q) {
+        const Group& g = o->groups[q];
+        const bool on = q < o->group_present.size() && o->group_present[q];
+        next[q] = g.step + (on ? 1 : 0);
+        if (!on) continue;
+        const double t = (double)next[q];
+        const double bc1 = 1.0 - std::pow(g.beta1, t);
+        const double bc2 = 1.0 - std::pow(g.beta2, t);
+        soma::GroupHp& hp = ua.groups[q];
+        hp.decay = (float)(1.0 - g.lr * g.weight_decay);
+        hp.beta1 = (float)g.beta1;
+        hp.one_minus_beta1 = (float)(1.0 - g.beta1);
+        hp.beta2 = (float)g.beta2;
+        hp.one_minus_beta2 = (float)(1.0 - g.beta2);
+        hp.step_size = (float)(g.lr / bc1);
+        hp.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+        hp.eps = (float)g.eps;
+    }
+    soma::NormArgs na{};
+    na.t = o->norm_tab;
+    na.partials = o->d_partials;
+    na.res = o->d_res;
+    na.divisor = grad_divisor;
+    na.max_norm = max_norm;
+
+    std::array<cudaEvent_t, 3>* ev = nullptr;
+    if (o->timing) {
+        if (o->tev_used == kTimingRing && (st = timing_flush(o)) != SOMA_OK) return st;
+        if (o->tev_used == o->tev.size()) {
+            std::array<cudaEvent_t, 3> t3{};
+            for (auto& x : t3)
+                if ((e = cudaEventCreate(&x)) != cudaSuccess) return o->cuda_fail(e, "cudaEventCreate(timing)");
+            o->tev.push_back(t3);
+        }
+        ev = &o->tev[o->tev_used];
+        if ((e = cudaEventRecord((*ev)[0], (cudaStream_t)stream)) != cudaSuccess)
+            return o->cuda_fail(e, "cudaEventRecord");
+    }
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream)) != cudaSuccess)
+        return o->cuda_fail(e, "launching the square-sum kernel");
+    if (ev && (e = cudaEventRecord((*ev)[1], (cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventRecord");
+    if (o->upd_grid > 0 && (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream)) != cudaSuccess)
+        return o->cuda_fail(e, "launching the update kernel");
+    if (ev) {
+        if ((e = cudaEventRecord((*ev)[2], (cudaStream_t)stream)) != cudaSuccess)
+            return o->cuda_fail(e, "cudaEventRecord");
+        o->tev_used += 1;
+    }
+    if ((e = cudaEventRecord(o->done, (cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventRecord");
+    o->have_done = true;
+    o->last_stream = stream;
+    for (size_t q = 0; q < o->groups.size(); ++q) o->groups[q].step = next[q];
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_get_norm(soma_opt_t h, double* norm, double* clip_coef, int32_t* nonfinite, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!o->have_done) return o->fail(SOMA_ERR_STATE, "no step has run on this handle");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    cudaError_t e;
+    if (o->last_stream != stream && (e = cudaStreamWaitEvent((cudaStream_t)stream, o->done, 0)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaStreamWaitEvent");
+    if ((e = cudaMemcpyAsync(o->h_res, o->d_res, sizeof(soma::Result), cudaMemcpyDeviceToHost,
+                             (cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMemcpyAsync(result)");
+    if ((e = cudaStreamSynchronize((cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaStreamSynchronize");
+    if (norm) *norm = o->h_res->norm;
+    if (clip_coef) *clip_coef = o->h_res->coef;
+    if (nonfinite) *nonfinite = (int32_t)o->h_res->nonfinite;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_set_timing(soma_opt_t h, int32_t enable) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (enable != 0 && enable != 1) return o->fail(SOMA_ERR_INVALID_ARG, "enable must be 0 or 1");
+    o->timing = enable != 0;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_read_timing(soma_opt_t h, double* norm_ms, double* update_ms, int64_t* steps) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (o->tev_used) {
+        DeviceGuard dg(o->device);
+        if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+        soma_status_t st = timing_flush(o);
+        if (st != SOMA_OK) return st;
+    }
+    if (norm_ms) *norm_ms = o->acc_norm_ms;
+    if (update_ms) *update_ms = o->acc_upd_ms;
+    if (steps) *steps = o->acc_steps;
+    o->acc_norm_ms = o->acc_upd_ms = 0.0;
+    o->acc_steps = 0;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_get_plan(soma_opt_t h, soma_plan_t* plan) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!plan) return o->fail(SOMA_ERR_INVALID_ARG, "plan is NULL");
+    *plan = o->plan;
+    return SOMA_OK;
+}
+
+void soma_opt_destroy(soma_opt_t h) {
+    soma_opt* o = live_handle(h);
+    if (!o) return;
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        g_live.erase(o);
+    }
+    if (o->dev_ready) {
+        DeviceGuard dg(o->device);
+        if (o->have_done) cudaEventSynchronize(o->done);
+        for (auto& t3 : o->tev)
+            for (auto& x : t3) cudaEventDestroy(x);
+        if (o->done) cudaEventDestroy(o->done);
+        if (o->d_res) cudaFree(o->d_res);
+        if (o->d_partials) cudaFree(o->d_partials);
+        if (o->d_tables) cudaFree(o->d_tables);
+        if (o->h_res) cudaFreeHost(o->h_res);
+        if (o->h_staging) cudaFreeHost(o->h_staging);
+    }
+    delete o;
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+"""GPU-vs-oracle harness shared by the parity tests.
+
+Device buffers are carved out of larger allocations with a sentinel guard
+band before and after every tensor; after each step the bands must be
+bit-unchanged (an out-of-bounds write shows up there).  Gradients and frozen
+tensors are compared bit for bit with copies taken before the step.
+
+Tolerances (per element, after every chained step): norm within 1e-5
+relative; p, m, v within 2e-6 * |ref| + 1e-8 of the fp64 oracle.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as W
+from oracle import GroupState, OracleOptimizer
+from tensor_grad_clip_gb300 import SomaOpt, TensorList
+
+NORM_RTOL = 1e-5
+RTOL = 2e-6
+ATOL = 1e-8
+PAD = 64                      # guard elements on each side (256 B for fp32)
+SENTINEL_F32 = 0x7FC0DEAD     # a NaN payload no computation produces
+SENTINEL_BF16 = 0x7FAD
+
+
+def assert_close(name, got, ref, rtol=RTOL, atol=ATOL):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    bound = rtol * np.abs(ref) + atol
+    bad = ~(err <= bound)
+    if bad.any():
+        i = int(np.argmax(np.where(bad, err / bound, 0)))
+        raise AssertionError(f"{name}: {int(bad.sum())} of {got.size} elements out of tolerance; worst at "
+                             f"{i}: got {got.flat[i]!r} ref {ref.flat[i]!r} err {err.flat[i]:.3e} "
+                             f"bound {bound.flat[i]:.3e}")
+
+
+class DeviceList:
+    """Device copies of a workload's weights, zero moments and gradient
+    buffers, each inside a guard-banded allocation.  `shift` moves every
+    buffer of tensor k by shift[k] = (p, g, m, v) elements off the 256-byte
+    grid (to exercise unaligned heads)."""
+
+    def __init__(self, w: W.Workload, params_cpu, device="cuda", shift=None, frozen_null=False):
+        self.w = w
+        self.device = device
+        self.bufs = []      # (full buffer, sentinel word, view slice)
+        self.p, self.g, self.m, self.v = [], [], [], []
+        for k, t in enumerate(w.tensors):
+            sp, sg, sm, sv = shift[k] if shift is not None else (0, 0, 0, 0)
+            gdt = W.torch_dtype(t.grad_dtype)
+            p = self._alloc(t.numel, torch.float32, sp)
+            p.copy_(params_cpu[k].reshape(-1).to(device))
+            g = self._alloc(t.numel, gdt, sg)
+            m = self._alloc(t.numel, torch.float32, sm)
+            v = self._alloc(t.numel, torch.float32, sv)
+            m.zero_()
+            v.zero_()
+            self.p.append(p)
+            self.g.append(g)
+            self.m.append(m)
+            self.v.append(v)
+        trainable = [t.trainable for t in w.tensors]
+        if frozen_null:
+            none = lambda xs: [x if tr else None for x, tr in zip(xs, trainable)]
+            self.tl = TensorList(self.p, none(self.g), none(self.m), none(self.v),
+                                 groups=[t.group for t in w.tensors], trainable=trainable,
+                                 owned=[t.owned for t in w.tensors])
+        else:
+            self.tl = TensorList(self.p, self.g, self.m, self.v, groups=[t.group for t in w.tensors],
+                                 trainable=trainable, owned=[t.owned for t in w.tensors])
+
+    def _alloc(self, numel, dtype, shift):
+        full = torch.empty(numel + 2 * PAD + 8, dtype=dtype, device=self.device)
+        word = SENTINEL_F32 if dtype == torch.float32 else SENTINEL_BF16
+        iview = full.view(torch.int32 if dtype == torch.float32 else torch.int16)
+        iview.fill_(word)
+        lo = PAD + shift
+        self.bufs.append((full, iview.clone(), lo, numel))
+        return full[lo:lo + numel]
+
+    def load_grads(self, grads):
+        for dst, src in zip(self.g, grads):
+            dst.copy_(src.reshape(-1))
+
+    def check_guards(self):
+        for full, pattern, lo, numel in self.bufs:
+            iv = full.view(pattern.dtype)
+            if not torch.equal(iv[:lo], pattern[:lo]) or not torch.equal(iv[lo + numel:], pattern[lo + numel:]):
+                raise AssertionError("a guard band around a tensor was overwritten")
+
+    def snapshot(self):
+        """Bit copies of every gradient and of frozen tensors' p, m, v."""
+        snap = {"g": [x.clone() for x in self.g]}
+        snap["frozen"] = [(k, self.p[k].clone(), self.m[k].clone(), self.v[k].clone())
+                          for k, t in enumerate(self.w.tensors) if not t.trainable]
+        return snap
+
+    def check_snapshot(self, snap):
+        for k, (a, b) in enumerate(zip(snap["g"], self.g)):
+            if not torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)):
+                raise AssertionError(f"gradient {k} changed")
+        for k, p, m, v in snap["frozen"]:
+            for x, y in ((p, self.p[k]), (m, self.m[k]), (v, self.v[k])):
+                if not torch.equal(x.view(torch.int32), y.view(torch.int32)):
+                    raise AssertionError(f"frozen tensor {k} changed")
+
+
+def make_opt(w: W.Workload, device_index=0) -> SomaOpt:
+    opt = SomaOpt(device_index)
+    for g in w.groups:
+        opt.add_group(lr=g.lr, betas=(g.beta1, g.beta2), eps=g.eps, weight_decay=g.weight_decay)
+    return opt
+
+
+def make_oracle(w: W.Workload, params_cpu) -> OracleOptimizer:
+    flags = [(t.group, t.trainable, t.owned) for t in w.tensors]
+    groups = [GroupState(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps, weight_decay=g.weight_decay)
+              for g in w.groups]
+    return OracleOptimizer([p.double().numpy().reshape(-1) for p in params_cpu], flags, groups)
+
+
+def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=None, check_every_step=True):
+    """Chained steps of `w` on the GPU and in the oracle, compared after
+    every step.  Returns the list of (gpu_norm, oracle_norm, gpu_coef,
+    oracle_coef) per step."""
+    steps = w.steps if steps is None else steps
+    params = W.draw_params(w, "cpu")
+    dl = DeviceList(w, params, shift=shift, frozen_null=frozen_null)
+    opt = make_opt(w)
+    if tuning:
+        opt.set_tuning(**tuning)
+    orc = make_oracle(w, params)
+    out = []
+    for s in range(1, steps + 1):
+        grads = W.draw_grads(w, s, "cpu")
+        dl.load_grads(grads)
+        lrs = w.group_lrs(s)
+        for q, lr in enumerate(lrs):
+            opt.set_lr(q, lr)
+            orc.set_lr(q, lr)
+        snap = dl.snapshot()
+        opt.step(dl.tl, w.grad_divisor, w.max_norm)
+        norm, coef, nonfinite = opt.get_norm()
+        rn, rc = orc.step(grads, w.grad_divisor, w.max_norm)
+        out.append((norm, rn, coef, rc))
+        assert not nonfinite
+        assert math.isclose(norm, rn, rel_tol=NORM_RTOL, abs_tol=1e-30), (s, norm, rn)
+        assert math.isclose(coef, rc, rel_tol=NORM_RTOL), (s, coef, rc)
+        if rc == 1.0:
+            assert coef == 1.0
+        dl.check_snapshot(snap)
+        dl.check_guards()
+        if check_every_step or s == steps:
+            for k, t in enumerate(w.tensors):
+                if not t.trainable:
+                    continue
+                assert_close(f"step {s} {t.name} p", dl.p[k].cpu().numpy(), orc.params[k])
+                assert_close(f"step {s} {t.name} m", dl.m[k].cpu().numpy(), orc.exp_avg[k])
+                assert_close(f"step {s} {t.name} v", dl.v[k].cpu().numpy(), orc.exp_avg_sq[k])
+        for q in range(len(w.groups)):
+            assert opt.get_group_step(q) == orc.groups[q].step
+    opt.close()
+    return out

@@ -34,6 +34,21 @@ def _normal(shape, std: float, seed: int, device, dtype) -> torch.Tensor:
     return x if dtype == torch.float32 else x.to(dtype)
 
 
+def draw_param(w: Workload, k: int, device="cpu") -> torch.Tensor:
+    """fp32 weight k of the workload, N(0, param_std)."""
+    return _normal(w.tensors[k].shape, w.param_std, tensor_seed(w.seed, "param", 0, k), device,
+                   torch.float32)
+
+
+def draw_grad(w: Workload, k: int, step: int, device="cpu") -> torch.Tensor:
+    """Gradient k of step `step` in its grad dtype (zeros if zero_grad)."""
+    t = w.tensors[k]
+    dt = _DTYPES[t.grad_dtype]
+    if t.zero_grad:
+        return torch.zeros(t.shape, device=device, dtype=dt)
+    return _normal(t.shape, w.grad_std, tensor_seed(w.seed, "grad", step, k), device, dt)
+
+
 def draw_params(w: Workload, device="cpu") -> list:
     """fp32 weights N(0, param_std) for every tensor, frozen ones included."""
     return [_normal(t.shape, w.param_std, tensor_seed(w.seed, "param", 0, i), device, torch.float32)
@@ -46,12 +61,8 @@ def draw_grads(w: Workload, step: int, device="cpu", out=None) -> list:
     gradients too, so that a test can check nobody reads or writes them.
     With `out`, values are written into those tensors instead."""
     res = []
-    for i, t in enumerate(w.tensors):
-        dt = _DTYPES[t.grad_dtype]
-        if t.zero_grad:
-            g = torch.zeros(t.shape, device=device, dtype=dt)
-        else:
-            g = _normal(t.shape, w.grad_std, tensor_seed(w.seed, "grad", step, i), device, dt)
+    for i in range(len(w.tensors)):
+        g = draw_grad(w, i, step, device)
         if out is not None:
             out[i].copy_(g)
             del g
