@@ -61,7 +61,7 @@ typedef int32_t soma_status_t;
 #define SOMA_ERR_OOM          5  /* device or pinned host allocation failed */
 #define SOMA_ERR_CUDA         6  /* a CUDA runtime call failed (detail in soma_opt_last_error) */
 #define SOMA_ERR_STATE        7  /* null or destroyed handle */
-#define SOMA_ERR_LIMIT        8  /* more groups than SOMA_MAX_GROUPS */
+#define SOMA_ERR_LIMIT        8  /* a fixed limit: SOMA_MAX_GROUPS, or the no-alloc scratch size */
 
 /* ---- gradient dtypes --------------------------------------------------- */
 #define SOMA_DTYPE_F32   0  /* IEEE binary32 */
@@ -181,6 +181,39 @@ int32_t soma_abi_version(void);
 /* Wait for the handle's outstanding work, free its device and host memory
  * and the handle.  NULL is ignored. */
 void soma_opt_destroy(soma_opt_t opt);
+
+/* ---- norm without allocation ---------------------------------------------
+ * No counterpart on the pages: this entry point exists for callers that may
+ * not allocate device memory -- an application whose own allocator owns the
+ * device heap (where an extra cudaMalloc fails or fragments its pool), or a
+ * latency-critical loop where cudaMalloc/cudaFree, which can synchronise the
+ * device, are not allowed.
+ *
+ * Computes, on `stream`, the same norm and clip coefficient as the first
+ * kernel of soma_opt_step (norm over trainable, owned entries of `list`,
+ * c = min(1, max_norm / (norm + 1e-6))) and writes them as two doubles
+ * {norm, c} to `out` (device memory, 8-byte aligned, caller-owned).  It
+ * updates nothing and needs no handle; only the entries' grad, grad_dtype,
+ * numel, trainable and owned fields are read.
+ *
+ * Scratch: a fixed array of SOMA_NOALLOC_SCRATCH_BYTES (4 MiB) in the
+ * library's device image, held by every GPU that loads the library until the
+ * process exits.  No cudaMalloc, cudaFree or other allocating call is made.
+ * A list whose tables and partial sums do not fit returns SOMA_ERR_LIMIT
+ * before anything is enqueued (with chunks of at least 32 Ki elements, about
+ * 20 000 owned entries fit, of any total size).
+ *
+ * The first call on a device, with that device made current, looks up the
+ * array's device address and keeps it; make that first call before any stream
+ * capture.  Every call shares the array and overwrites what the previous call
+ * left there (it clears the result block each time).  Calls that overlap on
+ * the GPU -- on unordered streams, or from several host threads -- race on
+ * the array: order them.  Returns SOMA_ERR_INVALID_ARG, SOMA_ERR_DTYPE,
+ * SOMA_ERR_ALIGNMENT, SOMA_ERR_LIMIT or SOMA_ERR_CUDA (no detail text). */
+#define SOMA_NOALLOC_SCRATCH_BYTES (4u << 20)
+soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tensor_t *list, int64_t n,
+                                     double grad_divisor, double max_norm, double *out,
+                                     void *stream);
 
 #ifdef __cplusplus
 }

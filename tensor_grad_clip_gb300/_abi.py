@@ -91,7 +91,10 @@ SIGNATURES = {
     "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),
     "soma_abi_version": (_I32, []),
     "soma_opt_destroy": (None, [soma_opt_t]),
+    "soma_clip_norm_noalloc": (soma_status_t, [_I32, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
 }
+SOMA_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lib = None
 

@@ -2,7 +2,7 @@
 
     python -m tensor_grad_clip_gb300.build [--force]
 
-Two translation units (kernels.cu, soma_opt.cpp) compile in parallel and link
+The translation units (kernels.cu, soma_opt.cpp, noalloc.cu) compile in parallel and link
 into tensor_grad_clip_gb300/_build/libsoma_opt.so with the CUDA runtime linked
 statically, so the library needs nothing but the driver at load time.
 """
@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libsoma_opt.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kernels.cu", "soma_opt.cpp"]
+SOURCES = ["kernels.cu", "soma_opt.cpp", "noalloc.cu"]
 HEADERS = ["soma_kernels.h"]
 
 

@@ -1,0 +1,195 @@
+// soma_clip_norm_noalloc: the global gradient norm and clip coefficient
+// without any memory allocation by the library.
+//
+// Some callers cannot allocate device memory: a host application or
+// framework that owns the whole device heap through its own allocator (a
+// stray cudaMalloc there fails once that allocator has reserved HBM, or
+// fragments its pool), and latency-critical loops in which cudaMalloc /
+// cudaFree, which may synchronise the device, are not allowed.  For them this
+// entry point runs the square-sum kernel with all of its scratch (the
+// arrival ticket and result, the per-chunk partial sums and the chunk /
+// segment tables) placed in one file-scope __device__ array of fixed size.
+// Every GPU that loads the library holds that array until the process exits.
+//
+// Set-up: the first call on a device, with that device current, looks up the
+// array's device address with cudaGetSymbolAddress (in host code the array's
+// name is only a host-side stand-in, not a device address) and caches it.
+// Make that first call before any stream capture.
+//
+// All calls share the one array, which keeps the contents of the last call:
+// every call rewrites the tables and clears the result/ticket block before
+// launching.  Calls whose work overlaps on the GPU (different streams with no
+// ordering between them, or several threads) race on the array; order them.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstddef>
+#include <cstring>
+#include <mutex>
+
+#include "soma_kernels.h"
+#include "soma_opt.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = SOMA_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+constexpr size_t kResultBytes = 256;         // soma::Result, padded
+constexpr int64_t kMinChunk = 32768;          // elements per chunk, at least
+constexpr int64_t kTargetChunks = 32768;      // grows the chunk for large lists
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+namespace {
+
+std::mutex g_mu;                               // one host-side user at a time
+alignas(256) unsigned char g_stage[kScratchBytes];  // host image of the scratch
+void* g_dev_scratch[kMaxDevices];              // per device: address of the array
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Counts (segs == nullptr) or writes the norm table: the
+// trainable, owned entries cut into segments, grouped into chunks of about
+// `chunk` elements and at most kMaxSegsPerChunk segments each.  The vector
+// head is the number of leading elements before the gradient is 16-byte
+// aligned.
+void norm_table(const soma_tensor_t* list, int64_t n, int64_t chunk, soma::Seg* segs, int32_t* begin,
+                int64_t* nseg_out, int64_t* nchunk_out) {
+    int64_t nseg = 0, nchunk = 0, cur_elems = 0;
+    int cur_segs = 0;
+    if (begin) begin[0] = 0;
+    for (int64_t k = 0; k < n; ++k) {
+        const soma_tensor_t& t = list[k];
+        if (!t.trainable || !t.owned || t.numel == 0) continue;
+        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
+        int h = -1;
+        for (int c = 0; c < soma::kVec && h < 0; ++c)
+            if (((uintptr_t)t.grad + (uintptr_t)c * gsz) % 16 == 0) h = c;
+        int64_t off = 0;
+        while (off < t.numel) {
+            if (cur_segs == soma::kMaxSegsPerChunk || cur_elems >= chunk) {
+                ++nchunk;
+                if (begin) begin[nchunk] = (int32_t)nseg;
+                cur_elems = 0;
+                cur_segs = 0;
+            }
+            int64_t cut = off + std::min(t.numel - off, chunk - cur_elems);
+            if (h >= 0 && cut < t.numel && cut > h) {
+                cut = h + (cut - h + soma::kVec - 1) / soma::kVec * soma::kVec;
+                if (cut > t.numel) cut = t.numel;
+            }
+            const int64_t len = cut - off;
+            if (segs) {
+                soma::Seg s{};
+                s.g = static_cast<const char*>(t.grad) + off * gsz;
+                s.len = (int32_t)len;
+                if (h < 0) {
+                    s.head = (int32_t)len;
+                    s.nvec = 0;
+                } else {
+                    s.head = off < h ? (int32_t)std::min<int64_t>(h - off, len) : 0;
+                    s.nvec = (int32_t)((len - s.head) / soma::kVec);
+                }
+                s.gdtype = t.grad_dtype;
+                segs[nseg] = s;
+            }
+            ++nseg;
+            cur_elems += len;
+            ++cur_segs;
+            off = cut;
+        }
+    }
+    if (cur_segs > 0) {
+        ++nchunk;
+        if (begin) begin[nchunk] = (int32_t)nseg;
+    }
+    *nseg_out = nseg;
+    *nchunk_out = nchunk;
+}
+
+struct CurrentDevice {
+    int prev = -1;
+    cudaError_t status = cudaSuccess;
+    explicit CurrentDevice(int dev) {
+        status = cudaGetDevice(&prev);
+        if (status == cudaSuccess && prev != dev) status = cudaSetDevice(dev);
+    }
+    ~CurrentDevice() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+extern "C" soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tensor_t* list, int64_t n,
+                                                double grad_divisor, double max_norm, double* out,
+                                                void* stream) {
+    if (device < 0 || device >= kMaxDevices || n < 0 || (n > 0 && !list) || !out ||
+        (uintptr_t)out % alignof(double) != 0)
+        return SOMA_ERR_INVALID_ARG;
+    if (!std::isfinite(grad_divisor) || grad_divisor <= 0 || !std::isfinite(max_norm) || max_norm <= 0)
+        return SOMA_ERR_INVALID_ARG;
+    int64_t owned = 0;
+    for (int64_t k = 0; k < n; ++k) {
+        const soma_tensor_t& t = list[k];
+        if (t.reserved != 0 || t.trainable > 1 || t.owned > 1 || t.numel < 0) return SOMA_ERR_INVALID_ARG;
+        if (!t.trainable || !t.owned || t.numel == 0) continue;
+        if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16) return SOMA_ERR_DTYPE;
+        if (!t.grad) return SOMA_ERR_INVALID_ARG;
+        if ((uintptr_t)t.grad % (t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2)) return SOMA_ERR_ALIGNMENT;
+        owned += t.numel;
+    }
+    int64_t chunk = std::max<int64_t>(kMinChunk, (owned + kTargetChunks - 1) / kTargetChunks);
+    chunk = (chunk + 63) / 64 * 64;
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int64_t nseg = 0, nchunk = 0;
+    norm_table(list, n, chunk, nullptr, nullptr, &nseg, &nchunk);
+    const size_t o_part = kResultBytes;
+    const size_t o_seg = o_part + up256((size_t)std::max<int64_t>(nchunk, 1) * sizeof(double));
+    const size_t o_beg = o_seg + up256((size_t)nseg * sizeof(soma::Seg));
+    const size_t bytes = o_beg + up256((size_t)(nchunk + 1) * sizeof(int32_t));
+    if (bytes > kScratchBytes) return SOMA_ERR_LIMIT;  // list needs more scratch than the array holds
+
+    CurrentDevice cd(device);
+    if (cd.status != cudaSuccess) return SOMA_ERR_CUDA;
+    if (!g_dev_scratch[device]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return SOMA_ERR_CUDA;
+        }
+        g_dev_scratch[device] = p;
+    }
+    unsigned char* d = static_cast<unsigned char*>(g_dev_scratch[device]);
+
+    std::memset(g_stage, 0, kResultBytes);  // result and arrival ticket start at zero
+    norm_table(list, n, chunk, reinterpret_cast<soma::Seg*>(g_stage + o_seg),
+               reinterpret_cast<int32_t*>(g_stage + o_beg), &nseg, &nchunk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The pageable source is staged by the driver before the call returns,
+    // so g_stage can be rewritten by the next call.
+    if (cudaMemcpyAsync(d, g_stage, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SOMA_ERR_CUDA;
+    }
+    soma::NormArgs a{};
+    a.t = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_seg), reinterpret_cast<const int32_t*>(d + o_beg),
+                      (int32_t)nchunk};
+    a.partials = reinterpret_cast<double*>(d + o_part);
+    a.res = reinterpret_cast<soma::Result*>(d);
+    a.divisor = grad_divisor;
+    a.max_norm = max_norm;
+    if (soma::launch_norm(a, (int)std::max<int64_t>(nchunk, 1), stream) != cudaSuccess) return SOMA_ERR_CUDA;
+    // norm and coef are adjacent in the result block
+    if (cudaMemcpyAsync(out, d + offsetof(soma::Result, norm), 2 * sizeof(double), cudaMemcpyDefault, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SOMA_ERR_CUDA;
+    }
+    return SOMA_OK;
+}
