@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tuning", default="", help="update_chunk,norm_chunk,ctas_per_sm")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="transformer blocks of the action-expert / shard-view lists (0 = full size)")
     return ap.parse_args()
 
 
@@ -127,10 +129,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def workload(name):
+def workload(name, blocks=0):
     import workloads as W
     if name not in W.FULL:
         raise SystemExit(f"unknown workload {name}; choose from {sorted(W.FULL)}")
+    if blocks and name == "action_expert":
+        return W.action_expert(n_blocks=blocks)
+    if blocks and name == "hsdp_shard":
+        return W.hsdp_shard_view(n_blocks=blocks)
     return W.FULL[name]()
 
 
@@ -239,7 +245,7 @@ def run_reference(args):
     import oracle
     import workloads as W
     from oracle import GroupState, OracleOptimizer
-    w = workload(args.workload)
+    w = workload(args.workload, args.blocks)
     oracle.lib()
     # calibrate: elements per second on one tensor, then size the per-step sample
     k0 = next(k for k, t in enumerate(w.tensors) if t.trainable)
@@ -293,7 +299,7 @@ def run_ours(args):
     import tensor_grad_clip_gb300
     tensor_grad_clip_gb300.load()
 
-    w = workload(args.workload)
+    w = workload(args.workload, args.blocks)
     flats, (p, g, m, v) = alloc_flat(w, device)
     opt = SomaOpt(local)
     for q in w.groups:
