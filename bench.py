@@ -158,33 +158,6 @@ def describe(w):
     }
 
 
-def alloc_flat(w, device):
-    """One flat device buffer per kind (p, g, m, v); each tensor is a view
-    starting on a 256-byte boundary.  Weights and gradients drawn on device."""
-    import torch
-    import workloads as W
-    offs, cur = [], 0
-    for t in w.tensors:
-        offs.append(cur)
-        cur += (t.numel + 63) // 64 * 64
-    total = max(cur, 64)
-    gdt = {W.torch_dtype(t.grad_dtype) for t in w.tensors}
-    if len(gdt) != 1:
-        raise SystemExit("bench expects one gradient dtype per workload")
-    gdt = gdt.pop()
-    P = torch.empty(total, dtype=torch.float32, device=device)
-    G = torch.zeros(total, dtype=gdt, device=device)
-    M = torch.zeros(total, dtype=torch.float32, device=device)
-    V = torch.zeros(total, dtype=torch.float32, device=device)
-    p, g, m, v = [], [], [], []
-    for k, t in enumerate(w.tensors):
-        sl = slice(offs[k], offs[k] + t.numel)
-        p.append(P[sl]); g.append(G[sl]); m.append(M[sl]); v.append(V[sl])
-        p[-1].copy_(W.draw_param(w, k, device).reshape(-1))
-        g[-1].copy_(W.draw_grad(w, k, 1, device).reshape(-1))
-    return (P, G, M, V), (p, g, m, v)
-
-
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("kernels.cu", "soma_kernels.h"):
@@ -297,10 +270,12 @@ def run_ours(args):
     device = torch.device("cuda", local)
     from tensor_grad_clip_gb300 import SomaOpt, TensorList
     import tensor_grad_clip_gb300
+    import workloads as W
     tensor_grad_clip_gb300.load()
 
     w = workload(args.workload, args.blocks)
-    flats, (p, g, m, v) = alloc_flat(w, device)
+    fb = W.FlatBuffers(w, device)
+    p, g, m, v = fb.p, fb.g, fb.m, fb.v
     opt = SomaOpt(local)
     for q in w.groups:
         opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
@@ -374,7 +349,7 @@ def run_ours(args):
     if not args.no_e2e:
         # End to end through the C ABI: every step copies that step's gradients
         # from pinned host memory and reads the norm back.
-        G = flats[1]
+        G = fb.G
         host_g = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
         host_g.copy_(G)
         torch.cuda.synchronize()

@@ -77,7 +77,24 @@ __device__ __forceinline__ double block_sum64(double x, double* scratch) {
     return r;
 }
 
-// ---- square-sum of one segment, accumulated into acc[0..1] --------------
+// ---- square-sum of one segment, accumulated into a0 / a1 -----------------
+
+__device__ __forceinline__ void sq8_bf16(const uint4 w, float& a0, float& a1) {
+    float x;
+    x = bf16_lo(w.x); a0 = fmaf(x, x, a0);
+    x = bf16_hi(w.x); a1 = fmaf(x, x, a1);
+    x = bf16_lo(w.y); a0 = fmaf(x, x, a0);
+    x = bf16_hi(w.y); a1 = fmaf(x, x, a1);
+    x = bf16_lo(w.z); a0 = fmaf(x, x, a0);
+    x = bf16_hi(w.z); a1 = fmaf(x, x, a1);
+    x = bf16_lo(w.w); a0 = fmaf(x, x, a0);
+    x = bf16_hi(w.w); a1 = fmaf(x, x, a1);
+}
+
+__device__ __forceinline__ void sq4_f32(const float4 u, float& a0, float& a1) {
+    a0 = fmaf(u.x, u.x, a0); a1 = fmaf(u.y, u.y, a1);
+    a0 = fmaf(u.z, u.z, a0); a1 = fmaf(u.w, u.w, a1);
+}
 
 __device__ __forceinline__ void sumsq_bf16(const Seg& s, float& a0, float& a1) {
     const uint16_t* g = static_cast<const uint16_t*>(s.g);
@@ -86,18 +103,17 @@ __device__ __forceinline__ void sumsq_bf16(const Seg& s, float& a0, float& a1) {
         a0 = fmaf(x, x, a0);
     }
     const uint4* gv = reinterpret_cast<const uint4*>(g + s.head);
-    for (int i = threadIdx.x; i < s.nvec; i += blockDim.x) {
-        uint4 w = __ldg(gv + i);
-        float x;
-        x = bf16_lo(w.x); a0 = fmaf(x, x, a0);
-        x = bf16_hi(w.x); a1 = fmaf(x, x, a1);
-        x = bf16_lo(w.y); a0 = fmaf(x, x, a0);
-        x = bf16_hi(w.y); a1 = fmaf(x, x, a1);
-        x = bf16_lo(w.z); a0 = fmaf(x, x, a0);
-        x = bf16_hi(w.z); a1 = fmaf(x, x, a1);
-        x = bf16_lo(w.w); a0 = fmaf(x, x, a0);
-        x = bf16_hi(w.w); a1 = fmaf(x, x, a1);
+    const int S = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + 3 * S < s.nvec; i += 4 * S) {  // four independent 16-byte loads in flight
+        const uint4 w0 = __ldg(gv + i), w1 = __ldg(gv + i + S);
+        const uint4 w2 = __ldg(gv + i + 2 * S), w3 = __ldg(gv + i + 3 * S);
+        sq8_bf16(w0, a0, a1);
+        sq8_bf16(w1, a0, a1);
+        sq8_bf16(w2, a0, a1);
+        sq8_bf16(w3, a0, a1);
     }
+    for (; i < s.nvec; i += S) sq8_bf16(__ldg(gv + i), a0, a1);
     for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
         float x = bf16_one(__ldg(g + j));
         a1 = fmaf(x, x, a1);
@@ -111,13 +127,19 @@ __device__ __forceinline__ void sumsq_f32(const Seg& s, float& a0, float& a1) {
         a0 = fmaf(x, x, a0);
     }
     const float4* gv = reinterpret_cast<const float4*>(g + s.head);
-    for (int i = threadIdx.x; i < s.nvec; i += blockDim.x) {
-        float4 u = __ldg(gv + 2 * i);
-        float4 w = __ldg(gv + 2 * i + 1);
-        a0 = fmaf(u.x, u.x, a0); a1 = fmaf(u.y, u.y, a1);
-        a0 = fmaf(u.z, u.z, a0); a1 = fmaf(u.w, u.w, a1);
-        a0 = fmaf(w.x, w.x, a0); a1 = fmaf(w.y, w.y, a1);
-        a0 = fmaf(w.z, w.z, a0); a1 = fmaf(w.w, w.w, a1);
+    const int S = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + S < s.nvec; i += 2 * S) {  // four independent 16-byte loads in flight
+        const float4 u0 = __ldg(gv + 2 * i), w0 = __ldg(gv + 2 * i + 1);
+        const float4 u1 = __ldg(gv + 2 * (i + S)), w1 = __ldg(gv + 2 * (i + S) + 1);
+        sq4_f32(u0, a0, a1);
+        sq4_f32(w0, a0, a1);
+        sq4_f32(u1, a0, a1);
+        sq4_f32(w1, a0, a1);
+    }
+    if (i < s.nvec) {
+        sq4_f32(__ldg(gv + 2 * i), a0, a1);
+        sq4_f32(__ldg(gv + 2 * i + 1), a0, a1);
     }
     for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
         float x = __ldg(g + j);
@@ -153,8 +175,19 @@ __global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant_
     if (!last) return;
     __threadfence();
 
+    // Thread t adds partials t, t + B, t + 2B, ... in that order (B = block
+    // size), eight loads in flight at a time; then a fixed-shape tree.
     double s = 0.0;
-    for (int i = threadIdx.x; i < a.t.nchunks; i += blockDim.x) s += __ldcg(a.partials + i);
+    const int n = a.t.nchunks, B = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + 7 * B < n; i += 8 * B) {
+        double x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = __ldcg(a.partials + i + u * B);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += x[u];
+    }
+    for (; i < n; i += B) s += __ldcg(a.partials + i);
     s = block_sum64<kNormBlock>(s, wsum64);
     if (threadIdx.x == 0) {
         const double norm = sqrt(s) / a.divisor;
@@ -262,10 +295,13 @@ __device__ __forceinline__ void update_body(const Seg& s, const GroupHp& h, floa
     }
 }
 
+// Chunks run in reverse list order: the gradients the square-sum kernel read
+// last are the ones most likely still in L2 when this kernel starts.
 __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_constant__ UpdateArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     const float scale = __ldcg(&a.res->scale);
-    for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
+    for (int r = blockIdx.x; r < a.t.nchunks; r += gridDim.x) {
+        const int c = a.t.nchunks - 1 - r;
         const int ns = stage_segments(a.t, c, segs);
         for (int k = 0; k < ns; ++k) {
             const Seg& s = segs[k];

@@ -24,7 +24,7 @@
 namespace {
 
 constexpr int32_t kDefaultUpdateChunk = 16384;
-constexpr int32_t kDefaultNormChunk = 32768;
+constexpr int32_t kDefaultNormChunk = 65536;
 constexpr size_t kTimingRing = 1024;
 
 struct Group {

@@ -1,0 +1,76 @@
+"""Flat device layout of a workload's buffers, as a training framework holds
+them: one buffer per kind (weights, gradients, first and second moments),
+each tensor a view starting on a 256-byte boundary.  The gaps between views
+are filled with a sentinel pattern so that a test can check nothing outside a
+tensor was written.  Values are drawn on the device (see generate.py)."""
+from __future__ import annotations
+
+import torch
+
+from .configs import Workload
+from .generate import draw_grad, draw_param, torch_dtype
+
+SENTINEL_F32 = 0x7FC0DEAD   # NaN payloads no arithmetic produces
+SENTINEL_BF16 = 0x7FAD
+ALIGN = 64                  # elements: 256 B of fp32, 128 B of bf16
+
+
+class FlatBuffers:
+    def __init__(self, w: Workload, device, grad_step: int = 1, gap: int = ALIGN):
+        self.w = w
+        self.device = torch.device(device)
+        self.offsets = []
+        cur = 0
+        for t in w.tensors:
+            self.offsets.append(cur)
+            cur += (t.numel + gap + ALIGN - 1) // ALIGN * ALIGN
+        total = max(cur, ALIGN)
+        gdts = {torch_dtype(t.grad_dtype) for t in w.tensors}
+        if len(gdts) != 1:
+            raise ValueError("one gradient dtype per flat workload")
+        self.grad_dtype = gdts.pop()
+        self.P = torch.empty(total, dtype=torch.float32, device=self.device)
+        self.G = torch.empty(total, dtype=self.grad_dtype, device=self.device)
+        self.M = torch.empty(total, dtype=torch.float32, device=self.device)
+        self.V = torch.empty(total, dtype=torch.float32, device=self.device)
+        for buf in (self.P, self.M, self.V):
+            buf.view(torch.int32).fill_(SENTINEL_F32)
+        if self.grad_dtype == torch.bfloat16:
+            self.G.view(torch.int16).fill_(SENTINEL_BF16)
+        else:
+            self.G.view(torch.int32).fill_(SENTINEL_F32)
+        self.p, self.g, self.m, self.v = [], [], [], []
+        for k, t in enumerate(w.tensors):
+            sl = slice(self.offsets[k], self.offsets[k] + t.numel)
+            self.p.append(self.P[sl])
+            self.g.append(self.G[sl])
+            self.m.append(self.M[sl])
+            self.v.append(self.V[sl])
+            self.p[-1].copy_(draw_param(w, k, self.device).reshape(-1))
+            self.m[-1].zero_()
+            self.v[-1].zero_()
+        self.load_grads(grad_step)
+
+    def load_grads(self, step: int):
+        for k in range(len(self.w.tensors)):
+            self.g[k].copy_(draw_grad(self.w, k, step, self.device).reshape(-1))
+
+    def gaps(self):
+        """(start, end) element ranges between and after the tensor views."""
+        out = []
+        for k, t in enumerate(self.w.tensors):
+            end = self.offsets[k + 1] if k + 1 < len(self.offsets) else self.P.numel()
+            if self.offsets[k] + t.numel < end:
+                out.append((self.offsets[k] + t.numel, end))
+        return out
+
+    def gaps_intact(self) -> bool:
+        gsent = SENTINEL_BF16 if self.grad_dtype == torch.bfloat16 else SENTINEL_F32
+        gi = self.G.view(torch.int16 if self.grad_dtype == torch.bfloat16 else torch.int32)
+        for a, b in self.gaps():
+            for buf in (self.P, self.M, self.V):
+                if not bool((buf.view(torch.int32)[a:b] == SENTINEL_F32).all()):
+                    return False
+            if not bool((gi[a:b] == gsent).all()):
+                return False
+        return True
