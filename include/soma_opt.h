@@ -203,6 +203,8 @@ void soma_opt_destroy(soma_opt_t opt);
  * before anything is enqueued (with chunks of at least 32 Ki elements, about
  * 20 000 owned entries fit, of any total size).
  *
+ * The call returns once the tables have been copied into the array (it waits
+ * on `stream` for that copy); the kernel and the copy to `out` stay queued.
  * The first call on a device, with that device made current, looks up the
  * array's device address and keeps it; make that first call before any stream
  * capture.  Every call shares the array and overwrites what the previous call

@@ -171,9 +171,11 @@ extern "C" soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tenso
     norm_table(list, n, chunk, reinterpret_cast<soma::Seg*>(g_stage + o_seg),
                reinterpret_cast<int32_t*>(g_stage + o_beg), &nseg, &nchunk);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The pageable source is staged by the driver before the call returns,
-    // so g_stage can be rewritten by the next call.
-    if (cudaMemcpyAsync(d, g_stage, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    // The copy may read g_stage only when it runs on the stream (the GPU can
+    // read pageable host memory directly on this platform), so wait for it
+    // before returning: the next call rewrites g_stage.
+    if (cudaMemcpyAsync(d, g_stage, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return SOMA_ERR_CUDA;
     }
