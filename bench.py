@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tuning", default="", help="update_chunk,norm_chunk,ctas_per_sm")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step (soma_opt_step_graph) in a CUDA graph and time its replays")
     ap.add_argument("--blocks", type=int, default=0,
                     help="transformer blocks of the action-expert / shard-view lists (0 = full size)")
     return ap.parse_args()
@@ -291,14 +293,30 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    for i in range(args.warmup):
-        lrs = w.group_lrs(i + 1)
-        for q, lr in enumerate(lrs):
-            opt.set_lr(q, lr)
-        opt.step(tl, w.grad_divisor, w.max_norm, stream)
+    graph = None
+    if args.graph:
+        # one step captured on a side stream; replays read lr and step counts
+        # from the library's device table
+        opt.push_groups(stream)
+        opt.step_graph(tl, w.grad_divisor, w.max_norm, stream)
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                opt.step_graph(tl, w.grad_divisor, w.max_norm, side)
+        torch.cuda.synchronize()
+        for i in range(args.warmup):
+            graph.replay()
+    else:
+        for i in range(args.warmup):
+            lrs = w.group_lrs(i + 1)
+            for q, lr in enumerate(lrs):
+                opt.set_lr(q, lr)
+            opt.step(tl, w.grad_divisor, w.max_norm, stream)
     torch.cuda.synchronize()
     plan = opt.plan()
-    opt.set_timing(True)
+    opt.set_timing(not args.graph)
     opt.read_timing()
 
     sampler = ClockSampler(local)
@@ -308,6 +326,9 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
+        if graph is not None:
+            graph.replay()
+            continue
         if w.lr_at is not None:
             for q, lr in enumerate(w.group_lrs(i % w.steps + 1)):
                 opt.set_lr(q, lr)
@@ -335,6 +356,8 @@ def run_ours(args):
     # dominant kernel: the fused update (26 B/elem bf16 grads, 28 B/elem fp32)
     upd_bytes = sum(t.numel * ((2 if t.grad_dtype == "bf16" else 4) + 24) for t in w.tensors if t.trainable)
     norm_bytes = sum(t.numel * (2 if t.grad_dtype == "bf16" else 4) for t in w.tensors if t.trainable and t.owned)
+    if graph is not None:  # no per-kernel events inside a graph: attribute the whole step
+        upd_ms, norm_ms, nsteps = elapsed_ms, 0.0, args.steps
     upd_avg_ms = upd_ms / max(nsteps, 1)
     norm_avg_ms = norm_ms / max(nsteps, 1)
     achieved = upd_bytes / (upd_avg_ms / 1e3) / 1e9
@@ -388,7 +411,8 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": describe(w) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                     "plan": plan},
+                                     "mode": "CUDA-graph replay of one step" if graph is not None
+                                     else "soma_opt_step per step", "plan": plan},
             "effective_hbm_gbs": eff_gbs * world,
             "effective_hbm_frac_of_peak": eff_gbs / hbm_peak,
             "effective_hbm_frac_of_8tbs": eff_gbs / 8000.0,

@@ -137,6 +137,51 @@ soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
 soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
                             double grad_divisor, double max_norm, void *stream);
 
+/* ---- graph-capturable step -------------------------------------------------
+ * The SomaSpeed page replays repeated learner work with CUDA graphs to cut
+ * launch overhead (its paragraph on compatible learner executions).  This
+ * variant of soma_opt_step can be captured in a CUDA graph and replayed: it
+ * enqueues only the two kernels, which read each group's hyperparameters and
+ * step count from a table in device memory and advance the step counts there
+ * (the square-sum kernel's last CTA does it, right after deriving c).
+ * grad_divisor and max_norm become part of a captured graph.
+ *
+ * Rules: soma_opt_push_groups must have run once; the first call with a list
+ * must happen outside capture (it builds and uploads the tables); from then
+ * on the handle keeps that list and its launch plan for its lifetime (other
+ * lists and soma_opt_set_tuning fail with SOMA_ERR_STATE; use another handle),
+ * so a captured graph never sees its tables move.  The host copy of the step
+ * counts is not advanced; soma_opt_pull_groups refreshes it. */
+soma_status_t soma_opt_step_graph(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
+                                  double grad_divisor, double max_norm, void *stream);
+
+/* Device table entry of one group (64 bytes); soma_opt_device_groups returns
+ * SOMA_MAX_GROUPS of them, indexed by group id. */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+    int64_t reserved[2];
+} soma_device_group_t;
+
+/* Copy the host-side hyperparameters of every group to the device table,
+ * and the host step count of each group whose count is newer than the
+ * device's (the first push, soma_opt_set_group_step, or regular steps since
+ * the last push); step counts that only graph steps advanced are kept.
+ * Enqueued on `stream` from library-owned pinned memory; not capturable; it
+ * waits only if its previous copy is still queued.  Call it after
+ * add/set_group/set_lr/set_group_step changes that graph steps should see. */
+soma_status_t soma_opt_push_groups(soma_opt_t opt, void *stream);
+
+/* Copy the device step counts back to the host copy, so that
+ * soma_opt_get_group_step reports graph steps (waits on `stream`; not
+ * capturable). */
+soma_status_t soma_opt_pull_groups(soma_opt_t opt, void *stream);
+
+/* Device address of the group table (library-owned, valid until destroy).
+ * A caller may write lr or other fields there between or inside graph
+ * replays, e.g. from its own learning-rate schedule kernel. */
+soma_status_t soma_opt_device_groups(soma_opt_t opt, soma_device_group_t **table);
+
 /* Norm and clip coefficient of the last step (fp64), and 1 if that norm was
  * not finite.  Any output pointer may be NULL.  Waits for the last step on
  * `stream`: the only call besides soma_opt_read_timing that blocks. */

@@ -157,12 +157,30 @@ class SomaOpt:
         self._check(_abi.soma_opt_step(self._h, tensors.pointer(), tensors.n, grad_divisor, max_norm,
                                        _stream_handle(stream)))
 
+    def step_graph(self, tensors: TensorList, grad_divisor: float, max_norm: float, stream=None):
+        """The graph-capturable step (soma_opt_step_graph): may be called
+        inside torch.cuda.graph capture once it has run outside capture."""
+        self._check(_abi.soma_opt_step_graph(self._h, tensors.pointer(), tensors.n, grad_divisor, max_norm,
+                                             _stream_handle(stream)))
+
+    def push_groups(self, stream=None):
+        self._check(_abi.soma_opt_push_groups(self._h, _stream_handle(stream)))
+
+    def pull_groups(self, stream=None):
+        self._check(_abi.soma_opt_pull_groups(self._h, _stream_handle(stream)))
+
+    def device_groups(self) -> int:
+        """Device address of the soma_device_group_t table."""
+        p = ctypes.c_void_p()
+        self._check(_abi.soma_opt_device_groups(self._h, ctypes.byref(p)))
+        return p.value
+
     def get_norm(self, stream=None):
         """(norm, clip_coef, nonfinite) of the last step; waits for it."""
         n, c, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_int32()
         self._check(_abi.soma_opt_get_norm(self._h, ctypes.byref(n), ctypes.byref(c), ctypes.byref(f),
                                            _stream_handle(stream)))
-        return n.value, c.value, bool(f.value)
+        return n.value, c.value, int(f.value)
 
     def set_timing(self, enable: bool):
         self._check(_abi.soma_opt_set_timing(self._h, 1 if enable else 0))

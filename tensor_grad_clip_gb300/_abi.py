@@ -64,6 +64,14 @@ class soma_plan_t(ctypes.Structure):
     ]
 
 
+class soma_device_group_t(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64),
+                ("reserved", ctypes.c_int64 * 2)]
+
+
+assert ctypes.sizeof(soma_device_group_t) == 64
+
 _D = ctypes.c_double
 _DP = ctypes.POINTER(ctypes.c_double)
 _I32 = ctypes.c_int32
@@ -91,6 +99,11 @@ SIGNATURES = {
     "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),
     "soma_abi_version": (_I32, []),
     "soma_opt_destroy": (None, [soma_opt_t]),
+    "soma_opt_step_graph": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,
+                                            ctypes.c_void_p]),
+    "soma_opt_push_groups": (soma_status_t, [soma_opt_t, ctypes.c_void_p]),
+    "soma_opt_pull_groups": (soma_status_t, [soma_opt_t, ctypes.c_void_p]),
+    "soma_opt_device_groups": (soma_status_t, [soma_opt_t, ctypes.POINTER(ctypes.c_void_p)]),
     "soma_clip_norm_noalloc": (soma_status_t, [_I32, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,
                                                ctypes.c_void_p, ctypes.c_void_p]),
 }

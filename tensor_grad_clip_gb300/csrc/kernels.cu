@@ -147,6 +147,24 @@ __device__ __forceinline__ void sumsq_f32(const Seg& s, float& a0, float& a1) {
     }
 }
 
+// Step constants of one group at step t, in fp64 rounded once to fp32 (the
+// same arithmetic as the host path of the regular step).
+__device__ __forceinline__ GroupHp group_constants(const DevGroup& g, int64_t t) {
+    const double bc1 = 1.0 - pow(g.beta1, (double)t);
+    const double bc2 = 1.0 - pow(g.beta2, (double)t);
+    GroupHp h;
+    h.decay = (float)(1.0 - g.lr * g.weight_decay);
+    h.beta1 = (float)g.beta1;
+    h.one_minus_beta1 = (float)(1.0 - g.beta1);
+    h.beta2 = (float)g.beta2;
+    h.one_minus_beta2 = (float)(1.0 - g.beta2);
+    h.step_size = (float)(g.lr / bc1);
+    h.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+    h.eps = (float)g.eps;
+    return h;
+}
+
+template <bool kGraph>
 __global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant__ NormArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     __shared__ float wsum[kNormBlock / 32];
@@ -199,6 +217,14 @@ __global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant_
         a.res->scale = (float)(coef / a.divisor);
         a.res->nonfinite = isfinite(norm) ? 0u : 1u;
         a.res->ticket = 0u;
+    }
+    if (kGraph) {
+        const int q = threadIdx.x;
+        if (q < a.ngroups && ((a.present >> q) & 1ull)) {
+            const int64_t t = a.dgroups[q].step + 1;
+            a.dgroups[q].step = t;
+            a.dhp[q] = group_constants(a.dgroups[q], t);
+        }
     }
 }
 
@@ -297,15 +323,20 @@ __device__ __forceinline__ void update_body(const Seg& s, const GroupHp& h, floa
 
 // Chunks run in reverse list order: the gradients the square-sum kernel read
 // last are the ones most likely still in L2 when this kernel starts.
+template <bool kGraph>
 __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_constant__ UpdateArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
+    __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
     const float scale = __ldcg(&a.res->scale);
+    if (kGraph) {  // made visible by the first __syncthreads in stage_segments
+        for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x) shp[q] = a.dhp[q];
+    }
     for (int r = blockIdx.x; r < a.t.nchunks; r += gridDim.x) {
         const int c = a.t.nchunks - 1 - r;
         const int ns = stage_segments(a.t, c, segs);
         for (int k = 0; k < ns; ++k) {
             const Seg& s = segs[k];
-            const GroupHp& h = a.groups[s.group];
+            const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
             for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one(s, j, h, scale);
             if (s.gdtype == kBF16) update_body<kBF16>(s, h, scale);
             else update_body<kF32>(s, h, scale);
@@ -318,13 +349,15 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
 
 }  // namespace
 
-int launch_norm(const NormArgs& a, int grid, void* stream) {
-    norm_kernel<<<grid, kNormBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+int launch_norm(const NormArgs& a, int grid, void* stream, bool graph) {
+    if (graph) norm_kernel<true><<<grid, kNormBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    else norm_kernel<false><<<grid, kNormBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return (int)cudaGetLastError();
 }
 
-int launch_update(const UpdateArgs& a, int grid, void* stream) {
-    update_kernel<<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph) {
+    if (graph) update_kernel<true><<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    else update_kernel<false><<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return (int)cudaGetLastError();
 }
 

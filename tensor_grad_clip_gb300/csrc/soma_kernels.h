@@ -68,6 +68,15 @@ struct Result {
 };
 static_assert(sizeof(Result) == 48, "Result layout");
 
+// Device copy of a group's hyperparameters and step count, used by the
+// graph-capturable step (the layout of soma_device_group_t in soma_opt.h).
+struct DevGroup {           // 64 bytes
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+    int64_t reserved[2];
+};
+static_assert(sizeof(DevGroup) == 64, "DevGroup layout");
+
 struct Table {
     const Seg* segs;
     const int32_t* chunk_begin;  // nchunks + 1 entries
@@ -80,19 +89,29 @@ struct NormArgs {
     Result* res;
     double divisor;
     double max_norm;
+    // graph-capturable step only: the last CTA advances the step count of
+    // every group whose bit is set in `present` and writes its constants
+    DevGroup* dgroups;
+    GroupHp* dhp;
+    uint64_t present;
+    int32_t ngroups;
 };
 
 struct UpdateArgs {
     Table t;
     const Result* res;
-    GroupHp groups[kMaxGroups];
+    GroupHp groups[kMaxGroups];   // regular step: constants as kernel arguments
+    const GroupHp* dhp;           // graph-capturable step: constants in device memory
+    int32_t ngroups;
 };
 
 constexpr int kNormBlock = 512;
 constexpr int kUpdateBlock = 256;
 
 // Launch wrappers (kernels.cu).  Return the cudaError_t of the launch as int.
-int launch_norm(const NormArgs& a, int grid, void* stream);
-int launch_update(const UpdateArgs& a, int grid, void* stream);
+// graph = true selects the variants that take group constants from device
+// memory (NormArgs::dgroups / dhp, UpdateArgs::dhp).
+int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false);
+int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false);
 
 }  // namespace soma

@@ -12,6 +12,7 @@
 #include <array>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -30,6 +31,7 @@ constexpr size_t kTimingRing = 1024;
 struct Group {
     double lr, beta1, beta2, eps, weight_decay;
     int64_t step;
+    bool step_dirty;  // the host count is newer than the device table's
 };
 
 thread_local std::string g_create_error;
@@ -68,6 +70,13 @@ struct soma_opt {
     cudaEvent_t done = nullptr;     // recorded after each step's last kernel
     bool have_done = false;
     void* last_stream = nullptr;
+    soma::DevGroup* d_groups = nullptr;  // graph-capturable step: group table
+    soma::GroupHp* d_hp = nullptr;       // and the constants of the current step
+    soma::DevGroup* h_groups = nullptr;  // pinned staging of the group table
+    cudaEvent_t groups_copied = nullptr; // last copy through h_groups finished
+    bool groups_copy_pending = false;
+    bool groups_pushed = false;
+    bool graph_locked = false;           // a graph step ran: the tables stay as they are
 
     // the list the device tables describe
     std::vector<soma_tensor_t> cached;
@@ -224,6 +233,17 @@ soma_status_t ensure_device(soma_opt* o) {
     if ((e = cudaMallocHost(&o->h_res, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMallocHost");
     if ((e = cudaEventCreateWithFlags(&o->done, cudaEventDisableTiming)) != cudaSuccess)
         return o->cuda_fail(e, "cudaEventCreate");
+    if ((e = cudaMalloc(&o->d_groups, soma::kMaxGroups * sizeof(soma::DevGroup))) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMalloc(groups)");
+    if ((e = cudaMalloc(&o->d_hp, soma::kMaxGroups * sizeof(soma::GroupHp))) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMalloc(group constants)");
+    if ((e = cudaMemset(o->d_groups, 0, soma::kMaxGroups * sizeof(soma::DevGroup))) != cudaSuccess ||
+        (e = cudaMemset(o->d_hp, 0, soma::kMaxGroups * sizeof(soma::GroupHp))) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMemset(groups)");
+    if ((e = cudaMallocHost(&o->h_groups, soma::kMaxGroups * sizeof(soma::DevGroup))) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMallocHost(groups)");
+    if ((e = cudaEventCreateWithFlags(&o->groups_copied, cudaEventDisableTiming)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventCreate");
     o->dev_ready = true;
     return SOMA_OK;
 }
@@ -345,6 +365,35 @@ soma_status_t timing_flush(soma_opt* o) {
 
 soma_opt* live_handle(soma_opt_t h) { return is_live(h) ? h : nullptr; }
 
+soma_status_t capturing(soma_opt* o, void* stream, bool* yes) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cs);
+    if (e != cudaSuccess) return o->cuda_fail(e, "cudaStreamIsCapturing");
+    *yes = cs != cudaStreamCaptureStatusNone;
+    return SOMA_OK;
+}
+
+// Common argument checks of the two step entry points; sets *same when the
+// list equals the cached one.
+soma_status_t check_step_args(soma_opt* o, const soma_tensor_t* list, int64_t n, double grad_divisor,
+                              double max_norm, bool* same) {
+    if (n < 0) return o->fail(SOMA_ERR_INVALID_ARG, "n < 0");
+    if (n > 0 && !list) return o->fail(SOMA_ERR_INVALID_ARG, "list is NULL with n > 0");
+    if (!is_finite(grad_divisor) || grad_divisor <= 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "grad_divisor must be finite and > 0 (got %g)", grad_divisor);
+    if (!is_finite(max_norm) || max_norm <= 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "max_norm must be finite and > 0 (got %g)", max_norm);
+    *same = o->cache_valid && (int64_t)o->cached.size() == n &&
+            (n == 0 || std::memcmp(o->cached.data(), list, (size_t)n * sizeof(soma_tensor_t)) == 0);
+    if (!*same) {
+        for (int64_t k = 0; k < n; ++k) {
+            soma_status_t st = validate_entry(o, list[k], k);
+            if (st != SOMA_OK) return st;
+        }
+    }
+    return SOMA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -405,7 +454,7 @@ soma_status_t soma_opt_add_group(soma_opt_t h, double lr, double beta1, double b
     if (st != SOMA_OK) return st;
     if ((int)o->groups.size() >= SOMA_MAX_GROUPS)
         return o->fail(SOMA_ERR_LIMIT, "at most %d parameter groups", SOMA_MAX_GROUPS);
-    o->groups.push_back(Group{lr, beta1, beta2, eps, weight_decay, 0});
+    o->groups.push_back(Group{lr, beta1, beta2, eps, weight_decay, 0, true});
     *group_id = (int32_t)o->groups.size() - 1;
     return SOMA_OK;
 }
@@ -464,6 +513,7 @@ soma_status_t soma_opt_set_group_step(soma_opt_t h, int32_t group, int64_t t) {
     if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
     if (t < 0) return o->fail(SOMA_ERR_INVALID_ARG, "step count must be >= 0");
     o->groups[group].step = t;
+    o->groups[group].step_dirty = true;
     return SOMA_OK;
 }
 
@@ -474,6 +524,7 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
     if (!ok_chunk(update_chunk) || !ok_chunk(norm_chunk))
         return o->fail(SOMA_ERR_INVALID_ARG, "chunk sizes must be 0 or in [64, 2^26]");
     if (ctas_per_sm < 0 || ctas_per_sm > 64) return o->fail(SOMA_ERR_INVALID_ARG, "ctas_per_sm must be in [0, 64]");
+    if (o->graph_locked) return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: its plan is fixed");
     o->update_chunk = update_chunk ? update_chunk / 64 * 64 : kDefaultUpdateChunk;
     o->norm_chunk = norm_chunk ? norm_chunk / 64 * 64 : kDefaultNormChunk;
     o->ctas_per_sm = ctas_per_sm;
@@ -485,22 +536,12 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
                             double max_norm, void* stream) {
     soma_opt* o = live_handle(h);
     if (!o) return SOMA_ERR_STATE;
-    if (n < 0) return o->fail(SOMA_ERR_INVALID_ARG, "n < 0");
-    if (n > 0 && !list) return o->fail(SOMA_ERR_INVALID_ARG, "list is NULL with n > 0");
-    if (!is_finite(grad_divisor) || grad_divisor <= 0)
-        return o->fail(SOMA_ERR_INVALID_ARG, "grad_divisor must be finite and > 0 (got %g)", grad_divisor);
-    if (!is_finite(max_norm) || max_norm <= 0)
-        return o->fail(SOMA_ERR_INVALID_ARG, "max_norm must be finite and > 0 (got %g)", max_norm);
-
     // An unchanged list was validated when it was cached (groups are never removed).
-    const bool same = o->cache_valid && (int64_t)o->cached.size() == n &&
-                      (n == 0 || std::memcmp(o->cached.data(), list, (size_t)n * sizeof(soma_tensor_t)) == 0);
-    if (!same) {
-        for (int64_t k = 0; k < n; ++k) {
-            soma_status_t st = validate_entry(o, list[k], k);
-            if (st != SOMA_OK) return st;
-        }
-    }
+    bool same = false;
+    soma_status_t st0 = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    if (st0 != SOMA_OK) return st0;
+    if (!same && o->graph_locked)
+        return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
 
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
@@ -575,7 +616,152 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
         return o->cuda_fail(e, "cudaEventRecord");
     o->have_done = true;
     o->last_stream = stream;
-    for (size_t q = 0; q < o->groups.size(); ++q) o->groups[q].step = next[q];
+    for (size_t q = 0; q < o->groups.size(); ++q) {
+        if (next[q] != o->groups[q].step) o->groups[q].step_dirty = true;
+        o->groups[q].step = next[q];
+    }
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,
+                                  double max_norm, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    bool same = false;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    if (st != SOMA_OK) return st;
+    if (!same && o->graph_locked)
+        return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    bool cap = false;
+    if ((st = capturing(o, stream, &cap)) != SOMA_OK) return st;
+    if (cap && (!o->dev_ready || !same))
+        return o->fail(SOMA_ERR_STATE, "run soma_opt_step_graph once with this list before capturing it");
+    if (!o->groups_pushed)
+        return o->fail(SOMA_ERR_STATE, "soma_opt_push_groups must run before the first graph-capturable step");
+    if ((st = ensure_device(o)) != SOMA_OK) return st;
+    cudaError_t e;
+    if (!cap && o->have_done && o->last_stream != stream &&
+        (e = cudaStreamWaitEvent((cudaStream_t)stream, o->done, 0)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaStreamWaitEvent");
+    if (!same) {
+        o->cache_valid = false;
+        if ((st = rebuild(o, list, n, stream)) != SOMA_OK) return st;
+    }
+    uint64_t present = 0;
+    for (size_t q = 0; q < o->group_present.size(); ++q)
+        if (o->group_present[q]) present |= 1ull << q;
+    soma::NormArgs na{};
+    na.t = o->norm_tab;
+    na.partials = o->d_partials;
+    na.res = o->d_res;
+    na.divisor = grad_divisor;
+    na.max_norm = max_norm;
+    na.dgroups = o->d_groups;
+    na.dhp = o->d_hp;
+    na.present = present;
+    na.ngroups = (int32_t)o->groups.size();
+    soma::UpdateArgs ua{};
+    ua.t = o->upd_tab;
+    ua.res = o->d_res;
+    ua.dhp = o->d_hp;
+    ua.ngroups = (int32_t)o->groups.size();
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, true)) != cudaSuccess)
+        return o->cuda_fail(e, "launching the square-sum kernel");
+    if (o->upd_grid > 0 && (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true)) != cudaSuccess)
+        return o->cuda_fail(e, "launching the update kernel");
+    o->graph_locked = true;
+    if (!cap) {
+        if ((e = cudaEventRecord(o->done, (cudaStream_t)stream)) != cudaSuccess)
+            return o->cuda_fail(e, "cudaEventRecord");
+        o->have_done = true;
+        o->last_stream = stream;
+    }
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_push_groups(soma_opt_t h, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    bool cap = false;
+    soma_status_t st = capturing(o, stream, &cap);
+    if (st != SOMA_OK) return st;
+    if (cap) return o->fail(SOMA_ERR_STATE, "soma_opt_push_groups cannot be captured");
+    if ((st = ensure_device(o)) != SOMA_OK) return st;
+    // The copy engine reads the staging buffer when the copy runs, not when it
+    // is enqueued: wait until the previous copy through it has finished.
+    cudaError_t e;
+    if (o->groups_copy_pending && (e = cudaEventSynchronize(o->groups_copied)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventSynchronize(groups)");
+    o->groups_copy_pending = false;
+    const size_t ng = o->groups.size();
+    for (size_t q = 0; q < ng; ++q) {
+        const Group& g = o->groups[q];
+        o->h_groups[q] = soma::DevGroup{g.lr, g.beta1, g.beta2, g.eps, g.weight_decay, g.step, {0, 0}};
+    }
+    if (ng > 0) {
+        // hyperparameters: the first 40 bytes of every 64-byte entry
+        const size_t hp_bytes = offsetof(soma::DevGroup, step);
+        if ((e = cudaMemcpy2DAsync(o->d_groups, sizeof(soma::DevGroup), o->h_groups, sizeof(soma::DevGroup),
+                                   hp_bytes, ng, cudaMemcpyHostToDevice, (cudaStream_t)stream)) != cudaSuccess)
+            return o->cuda_fail(e, "cudaMemcpy2DAsync(groups)");
+        // step counts only where the host count is newer (first push,
+        // soma_opt_set_group_step, regular steps): graph steps advance the
+        // device count and must not be rolled back
+        for (size_t q = 0; q < ng; ++q) {
+            if (!o->groups[q].step_dirty) continue;
+            if ((e = cudaMemcpyAsync(&o->d_groups[q].step, &o->h_groups[q].step, sizeof(int64_t),
+                                     cudaMemcpyHostToDevice, (cudaStream_t)stream)) != cudaSuccess)
+                return o->cuda_fail(e, "cudaMemcpyAsync(group step)");
+            o->groups[q].step_dirty = false;
+        }
+        if ((e = cudaEventRecord(o->groups_copied, (cudaStream_t)stream)) != cudaSuccess)
+            return o->cuda_fail(e, "cudaEventRecord(groups)");
+        o->groups_copy_pending = true;
+    }
+    o->groups_pushed = true;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_pull_groups(soma_opt_t h, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!o->groups_pushed) return o->fail(SOMA_ERR_STATE, "no group table on the device yet");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    bool cap = false;
+    soma_status_t st = capturing(o, stream, &cap);
+    if (st != SOMA_OK) return st;
+    if (cap) return o->fail(SOMA_ERR_STATE, "soma_opt_pull_groups cannot be captured");
+    cudaError_t e;
+    if (o->groups_copy_pending && (e = cudaEventSynchronize(o->groups_copied)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventSynchronize(groups)");
+    o->groups_copy_pending = false;
+    const size_t ng = o->groups.size();
+    if (ng > 0 && (e = cudaMemcpyAsync(o->h_groups, o->d_groups, ng * sizeof(soma::DevGroup),
+                                       cudaMemcpyDeviceToHost, (cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMemcpyAsync(groups)");
+    if ((e = cudaStreamSynchronize((cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaStreamSynchronize");
+    for (size_t q = 0; q < ng; ++q) {
+        o->groups[q].step = o->h_groups[q].step;
+        o->groups[q].step_dirty = false;
+    }
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_device_groups(soma_opt_t h, soma_device_group_t** table) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!table) return o->fail(SOMA_ERR_INVALID_ARG, "table is NULL");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    soma_status_t st = ensure_device(o);
+    if (st != SOMA_OK) return st;
+    *table = reinterpret_cast<soma_device_group_t*>(o->d_groups);
     return SOMA_OK;
 }
 
@@ -642,14 +828,19 @@ void soma_opt_destroy(soma_opt_t h) {
     if (o->dev_ready) {
         DeviceGuard dg(o->device);
         if (o->have_done) cudaEventSynchronize(o->done);
+        if (o->groups_copy_pending) cudaEventSynchronize(o->groups_copied);
         for (auto& t3 : o->tev)
             for (auto& x : t3) cudaEventDestroy(x);
         if (o->done) cudaEventDestroy(o->done);
         if (o->d_res) cudaFree(o->d_res);
         if (o->d_partials) cudaFree(o->d_partials);
         if (o->d_tables) cudaFree(o->d_tables);
+        if (o->d_groups) cudaFree(o->d_groups);
+        if (o->d_hp) cudaFree(o->d_hp);
         if (o->h_res) cudaFreeHost(o->h_res);
         if (o->h_staging) cudaFreeHost(o->h_staging);
+        if (o->h_groups) cudaFreeHost(o->h_groups);
+        if (o->groups_copied) cudaEventDestroy(o->groups_copied);
     }
     delete o;
 }
