@@ -207,9 +207,10 @@ typedef struct {
 soma_status_t soma_opt_get_plan(soma_opt_t opt, soma_plan_t *plan);
 
 /* Tuning knobs for benchmarks: elements per update chunk and per norm chunk
- * (rounded to a multiple of 64; 0 keeps the default) and resident CTAs per
- * SM for a persistent grid (0 = one CTA per chunk).  Takes effect at the next
- * list (re)build. */
+ * (rounded to a multiple of 64; 0 = automatic: 16 Ki / 64 Ki elements, less
+ * for lists too small to give every SM four chunks, never below 1 Ki) and
+ * resident CTAs per SM for a persistent grid (0 = one CTA per chunk).  Takes
+ * effect at the next list (re)build. */
 soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t norm_chunk,
                                   int32_t ctas_per_sm);
 

@@ -26,6 +26,8 @@ namespace {
 
 constexpr int32_t kDefaultUpdateChunk = 16384;
 constexpr int32_t kDefaultNormChunk = 65536;
+constexpr int64_t kMinAutoChunk = 1024;   // smallest chunk the automatic sizing picks
+constexpr int64_t kAutoChunksPerSm = 4;   // small lists: aim for this many chunks per SM
 constexpr size_t kTimingRing = 1024;
 
 struct Group {
@@ -52,8 +54,8 @@ struct soma_opt {
     std::vector<Group> groups;
     std::string err;
 
-    int32_t update_chunk = kDefaultUpdateChunk;
-    int32_t norm_chunk = kDefaultNormChunk;
+    int32_t update_chunk = 0;       // 0: automatic (see chunk_size)
+    int32_t norm_chunk = 0;
     int32_t ctas_per_sm = 0;
 
     // device state, created on first use
@@ -256,8 +258,24 @@ soma_status_t wait_idle(soma_opt* o) {
     return e == cudaSuccess ? SOMA_OK : o->cuda_fail(e, "cudaEventSynchronize");
 }
 
+// Elements per chunk: the caller's choice, else the default, shrunk for
+// lists too small to give every SM a few chunks (down to kMinAutoChunk), so
+// that small lists still spread over the whole GPU.
+int64_t chunk_size(int32_t requested, int32_t dflt, int64_t total, int sm_count) {
+    if (requested > 0) return requested;
+    const int64_t spread = (total / (kAutoChunksPerSm * std::max(sm_count, 1)) + 63) / 64 * 64;
+    return std::max<int64_t>(kMinAutoChunk, std::min<int64_t>(dflt, spread));
+}
+
 soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* stream) {
-    TableBuilder upd(o->update_chunk), nrm(o->norm_chunk);
+    int64_t trainable_total = 0, owned_total = 0;
+    for (int64_t k = 0; k < n; ++k) {
+        if (!list[k].trainable) continue;
+        trainable_total += list[k].numel;
+        if (list[k].owned) owned_total += list[k].numel;
+    }
+    TableBuilder upd(chunk_size(o->update_chunk, kDefaultUpdateChunk, trainable_total, o->sm_count));
+    TableBuilder nrm(chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total, o->sm_count));
     std::vector<uint8_t> present(o->groups.size(), 0);
     int64_t trainable = 0, owned = 0;
     for (int64_t k = 0; k < n; ++k) {
@@ -525,8 +543,8 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
         return o->fail(SOMA_ERR_INVALID_ARG, "chunk sizes must be 0 or in [64, 2^26]");
     if (ctas_per_sm < 0 || ctas_per_sm > 64) return o->fail(SOMA_ERR_INVALID_ARG, "ctas_per_sm must be in [0, 64]");
     if (o->graph_locked) return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: its plan is fixed");
-    o->update_chunk = update_chunk ? update_chunk / 64 * 64 : kDefaultUpdateChunk;
-    o->norm_chunk = norm_chunk ? norm_chunk / 64 * 64 : kDefaultNormChunk;
+    o->update_chunk = update_chunk / 64 * 64;
+    o->norm_chunk = norm_chunk / 64 * 64;
     o->ctas_per_sm = ctas_per_sm;
     o->cache_valid = false;
     return SOMA_OK;
