@@ -4,9 +4,9 @@ TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
 CPU-baseline leg use it; the product library never imports it.  Nothing here
 imports the product package.
 
-Gradients are handed over in their stored type (fp32, or bf16 as raw 16-bit
-words), weights and moments as fp64 numpy arrays that the oracle updates in
-place.
+Gradients are handed over in their stored type (fp32, or bf16 / fp16 as raw
+16-bit words), weights and moments as fp64 numpy arrays that the oracle
+updates in place.
 """
 from __future__ import annotations
 
@@ -19,6 +19,7 @@ from . import build as _build
 
 GRAD_F32 = 0
 GRAD_BF16 = 1
+GRAD_F16 = 2
 
 _lib = None
 
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                           ctypes.c_double, ctypes.c_double, ctypes.c_int64,
                                           ctypes.c_double, ctypes.c_double]
+        L.oracle_f16_to_f64.restype = None
+        L.oracle_f16_to_f64.argtypes = [ctypes.c_void_p, dp, ctypes.c_int64]
         L.oracle_step.restype = ctypes.c_int
         L.oracle_step.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int64, ctypes.POINTER(_Group),
                                   ctypes.c_int32, ctypes.c_double, ctypes.c_double, dp, dp]
@@ -73,7 +76,8 @@ def lib() -> ctypes.CDLL:
 
 def grad_words(g) -> tuple:
     """(numpy array, dtype code) for a CPU gradient given as a torch tensor
-    (float32 or bfloat16) or a numpy array (float32, or uint16 bf16 words)."""
+    (float32, bfloat16 or float16) or a numpy array (float32, float16, or
+    uint16 bf16 words)."""
     try:
         import torch
         if isinstance(g, torch.Tensor):
@@ -82,6 +86,8 @@ def grad_words(g) -> tuple:
                 return g.numpy(), GRAD_F32
             if g.dtype == torch.bfloat16:
                 return g.view(torch.int16).numpy().view(np.uint16), GRAD_BF16
+            if g.dtype == torch.float16:
+                return g.view(torch.int16).numpy().view(np.uint16), GRAD_F16
             raise TypeError(f"unsupported gradient dtype {g.dtype}")
     except ImportError:  # pragma: no cover
         pass
@@ -90,7 +96,17 @@ def grad_words(g) -> tuple:
         return g, GRAD_F32
     if g.dtype == np.uint16:
         return g, GRAD_BF16
+    if g.dtype == np.float16:
+        return g.view(np.uint16), GRAD_F16
     raise TypeError(f"unsupported gradient dtype {g.dtype}")
+
+
+def f16_to_f64(words) -> np.ndarray:
+    """binary16 words (uint16) to fp64 through the oracle's own decoder."""
+    w = np.ascontiguousarray(words, dtype=np.uint16).reshape(-1)
+    out = np.empty(w.size, dtype=np.float64)
+    lib().oracle_f16_to_f64(w.ctypes.data, _dptr(out), w.size)
+    return out
 
 
 def _dptr(a: np.ndarray):

@@ -31,8 +31,9 @@
  *     p = p - lr * (m / bc1) / (sqrt(v / bc2) + eps),
  * with bc_k = 1 - b_k^t and t the group's step count after incrementing.
  *
- * Gradients are read in their stored type (fp32, or bf16 bits); both convert
- * to fp64 exactly.
+ * Gradients are read in their stored type (fp32, or bf16 or fp16 bits); all
+ * convert to fp64 exactly.  fp16 gradients are the compute-dtype gradients
+ * of an fp16 policy (RLinf page, "Retaining Low-Precision Gradients").
  */
 #include <math.h>
 #include <stdint.h>
@@ -40,6 +41,7 @@
 
 #define ORACLE_GRAD_F32 0
 #define ORACLE_GRAD_BF16 1
+#define ORACLE_GRAD_F16 2
 
 typedef struct {
     double *param;      /* fp64 weights, updated in place                */
@@ -58,16 +60,40 @@ typedef struct {
     int64_t step; /* steps this group has taken so far */
 } oracle_group;
 
+/* IEEE 754 binary16 word -> exact fp64: 1 sign bit, 5 exponent bits (bias
+ * 15), 10 fraction bits; exponent 0 is subnormal, 31 is inf/NaN. */
+static double half_to_double(uint16_t w)
+{
+    int sign = (w >> 15) & 1, e = (w >> 10) & 0x1f, f = w & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
 /* One stored gradient element as an exact fp64 value.  bf16 is the upper
  * half of an IEEE binary32, so widening it is a 16-bit shift. */
 static double grad_element(const void *grad, int32_t dtype, int64_t i)
 {
     if (dtype == ORACLE_GRAD_F32)
         return (double)((const float *)grad)[i];
+    if (dtype == ORACLE_GRAD_F16)
+        return half_to_double(((const uint16_t *)grad)[i]);
     uint32_t bits = ((uint32_t)((const uint16_t *)grad)[i]) << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
     return (double)f;
+}
+
+/* Exposed for the decoder's pin: n binary16 words to fp64. */
+void oracle_f16_to_f64(const uint16_t *w, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = half_to_double(w[i]);
 }
 
 /* Sum over one tensor of the squared normalized gradient, (g_i / d)^2. */

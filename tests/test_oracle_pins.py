@@ -338,3 +338,17 @@ def test_nonfinite_gradient_follows_the_library(bad):
     for k in range(2):
         np.testing.assert_allclose(opt.params[k], ref_p[k], rtol=1e-12, equal_nan=True)
         np.testing.assert_allclose(opt.exp_avg[k], ref_m[k], rtol=1e-12, equal_nan=True)
+
+
+def test_binary16_decoder_all_words():
+    # Every one of the 65 536 binary16 words against numpy's float16 (NaN
+    # words must decode to NaN, signed zeros keep their sign).
+    words = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f16_to_f64(words)
+    ref = words.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+    t = torch.tensor([1.0, -2.5, 6.1e-5, 65504.0], dtype=torch.float16)
+    assert oracle.tensor_sqsum(t, 2.0) == sum((float(x) / 2.0) ** 2 for x in t.float())
