@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--tuning", default="", help="update_chunk,norm_chunk,ctas_per_sm")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step (soma_opt_step_graph) in a CUDA graph and time its replays")
+    ap.add_argument("--master", action="store_true",
+                    help="action-expert list with bf16 model weights rewritten from fp32 master weights")
     ap.add_argument("--blocks", type=int, default=0,
                     help="transformer blocks of the action-expert / shard-view lists (0 = full size)")
     return ap.parse_args()
@@ -131,12 +133,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def workload(name, blocks=0):
+def workload(name, blocks=0, master=False):
     import workloads as W
     if name not in W.FULL:
         raise SystemExit(f"unknown workload {name}; choose from {sorted(W.FULL)}")
-    if blocks and name == "action_expert":
-        return W.action_expert(n_blocks=blocks)
+    if name == "action_expert" and (blocks or master):
+        return W.action_expert(n_blocks=blocks or 18, master=master)
     if blocks and name == "hsdp_shard":
         return W.hsdp_shard_view(n_blocks=blocks)
     return W.FULL[name]()
@@ -275,7 +277,7 @@ def run_ours(args):
     import workloads as W
     tensor_grad_clip_gb300.load()
 
-    w = workload(args.workload, args.blocks)
+    w = workload(args.workload, args.blocks, args.master)
     fb = W.FlatBuffers(w, device)
     p, g, m, v = fb.p, fb.g, fb.m, fb.v
     opt = SomaOpt(local)
@@ -285,8 +287,21 @@ def run_ours(args):
         uc, nc, cps = (int(x) for x in args.tuning.split(","))
         opt.set_tuning(uc, nc, cps)
     tl = TensorList(p, g, m, v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
-                    owned=[t.owned for t in w.tensors])
+                    owned=[t.owned for t in w.tensors], params_lowp=fb.plow)
     stream = torch.cuda.current_stream(device)
+    sharded_step = None
+    if world > 1:
+        # each rank holds its own shard of the list; the ranks exchange one
+        # float64 per step (their owned square-sums) for the global norm
+        from tensor_grad_clip_gb300.sharded import ShardedStep
+        sharded_step = ShardedStep(opt)
+
+    def one_step():
+        if sharded_step is not None:
+            sharded_step(tl, w.grad_divisor, w.max_norm)
+        else:
+            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+
     torch.cuda.synchronize()
 
     def barrier():
@@ -313,7 +328,7 @@ def run_ours(args):
             lrs = w.group_lrs(i + 1)
             for q, lr in enumerate(lrs):
                 opt.set_lr(q, lr)
-            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+            one_step()
     torch.cuda.synchronize()
     plan = opt.plan()
     opt.set_timing(not args.graph)
@@ -332,7 +347,7 @@ def run_ours(args):
         if w.lr_at is not None:
             for q, lr in enumerate(w.group_lrs(i % w.steps + 1)):
                 opt.set_lr(q, lr)
-        opt.step(tl, w.grad_divisor, w.max_norm, stream)
+        one_step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -354,8 +369,9 @@ def run_ours(args):
     alg_gbs = w.algorithmic_bytes_per_step() / (ms_per_step / 1e3) / 1e9
 
     # dominant kernel: the fused update (26 B/elem bf16 grads, 28 B/elem fp32)
-    upd_bytes = sum(t.numel * ((2 if t.grad_dtype == "bf16" else 4) + 24) for t in w.tensors if t.trainable)
-    norm_bytes = sum(t.numel * (2 if t.grad_dtype == "bf16" else 4) for t in w.tensors if t.trainable and t.owned)
+    gsz = lambda t: 4 if t.grad_dtype == "f32" else 2
+    upd_bytes = sum(t.numel * (gsz(t) + 24 + (2 if t.param_lowp else 0)) for t in w.tensors if t.trainable)
+    norm_bytes = sum(t.numel * gsz(t) for t in w.tensors if t.trainable and t.owned)
     if graph is not None:  # no per-kernel events inside a graph: attribute the whole step
         upd_ms, norm_ms, nsteps = elapsed_ms, 0.0, args.steps
     upd_avg_ms = upd_ms / max(nsteps, 1)
@@ -378,7 +394,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         for _ in range(2):
             G.copy_(host_g, non_blocking=True)
-            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+            one_step()
             opt.get_norm(stream)
         barrier()
         torch.cuda.synchronize()
@@ -386,7 +402,7 @@ def run_ours(args):
         e0.record(stream)
         for _ in range(args.e2e_steps):
             G.copy_(host_g, non_blocking=True)
-            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+            one_step()
             opt.get_norm(stream)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -410,7 +426,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": describe(w) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "config": describe(w) | {"parallelism": f"shard group x{world}: one all-gather of 8 B per rank per step"
+                                     if world > 1 else "single GPU",
                                      "mode": "CUDA-graph replay of one step" if graph is not None
                                      else "soma_opt_step per step", "plan": plan},
             "effective_hbm_gbs": eff_gbs * world,

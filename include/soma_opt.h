@@ -66,41 +66,48 @@ typedef int32_t soma_status_t;
 /* ---- gradient dtypes --------------------------------------------------- */
 #define SOMA_DTYPE_F32   0  /* IEEE binary32 */
 #define SOMA_DTYPE_BF16  1  /* bfloat16: the upper 16 bits of a binary32 */
+#define SOMA_DTYPE_F16   2  /* IEEE binary16 */
 
 #define SOMA_MAX_GROUPS  64
-#define SOMA_ABI_VERSION 1
+#define SOMA_ABI_VERSION 2
 
 typedef struct soma_opt soma_opt;
 typedef soma_opt *soma_opt_t;
 
-/* One entry of the tensor list (48 bytes, no implicit padding).
+/* One entry of the tensor list (56 bytes, no implicit padding).
  * All buffers are contiguous 1-D views of `numel` elements in device memory
  * (torch's Tensor.data_ptr() of a contiguous tensor).
- *   param       fp32 weights, updated in place; 4-byte aligned.
+ *   param       fp32 weights, updated in place; 4-byte aligned.  With
+ *               param_lowp set these are the fp32 master weights.
  *   grad        gradient in grad_dtype; NEVER written; aligned to its element size.
  *   exp_avg     fp32 first moment m, updated in place (zeros before step 1).
  *   exp_avg_sq  fp32 second moment v, updated in place (zeros before step 1).
+ *   param_lowp  optional (NULL = none): the model's bf16 or fp16 copy of the
+ *               weights, overwritten in the same pass with the updated fp32
+ *               weights rounded to nearest even (RLinf's FP32MasterAdamW:
+ *               bf16/fp16 parameters with an fp32 master copy); 2-byte aligned.
  *   numel       >= 0.
  *   group       id from soma_opt_add_group; ignored when frozen.
- *   grad_dtype  SOMA_DTYPE_*; ignored when frozen.
+ *   grad_dtype  SOMA_DTYPE_F32, _BF16 or _F16; ignored when frozen.
  *   trainable   0 = frozen: never read, never written, not in the norm; its
  *               pointers may be NULL.  1 = trainable.
  *   owned       1 = this rank owns the tensor (shard): it enters the norm.
  *               0 = replicated copy: updated with the same c, not in the norm.
- *   reserved    must be 0.
- * Buffers of different entries, and param/grad/exp_avg/exp_avg_sq of one
- * entry, must not overlap. */
+ *   lowp_dtype  SOMA_DTYPE_BF16 or _F16 when param_lowp is set, else 0.
+ * Buffers of different entries, and the buffers of one entry, must not
+ * overlap. */
 typedef struct {
     float *param;
     const void *grad;
     float *exp_avg;
     float *exp_avg_sq;
+    void *param_lowp;
     int64_t numel;
     int32_t group;
     uint8_t grad_dtype;
     uint8_t trainable;
     uint8_t owned;
-    uint8_t reserved;
+    uint8_t lowp_dtype;
 } soma_tensor_t;
 
 /* Create a handle bound to CUDA device `device`.  Makes no CUDA call: device
@@ -181,6 +188,30 @@ soma_status_t soma_opt_pull_groups(soma_opt_t opt, void *stream);
  * A caller may write lr or other fields there between or inside graph
  * replays, e.g. from its own learning-rate schedule kernel. */
 soma_status_t soma_opt_device_groups(soma_opt_t opt, soma_device_group_t **table);
+
+/* ---- multi-rank step (shard groups) -----------------------------------------
+ * With FSDP/HSDP each rank owns some shards; the SomaSpeed page takes one
+ * global clipping decision in which every shard counts once (its optimizer
+ * paragraph "SomaSpeed batches that work across tensors ...").  The only data
+ * the ranks exchange is one double per rank:
+ *
+ *   1. soma_opt_sumsq: this rank's sum over its trainable, owned entries of
+ *      (g/d)^2, written by the square-sum kernel to sumsq_out (device memory);
+ *   2. the caller gathers the ranks' values into one device array, rank r at
+ *      index r (e.g. an all-gather over the shard group);
+ *   3. soma_opt_step_from_sumsq: adds rank_sumsq[0..nranks) in index order,
+ *      so every rank derives the same norm and c bit for bit, then runs the
+ *      fused update on this rank's list.  Group step counts advance as in
+ *      soma_opt_step; soma_opt_get_norm reports the global norm.
+ *
+ * Both calls are asynchronous on `stream`; a replicated tensor must be owned
+ * by exactly one rank of the group. */
+#define SOMA_MAX_RANKS 65536
+soma_status_t soma_opt_sumsq(soma_opt_t opt, const soma_tensor_t *list, int64_t n, double grad_divisor,
+                             double *sumsq_out, void *stream);
+soma_status_t soma_opt_step_from_sumsq(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
+                                       double grad_divisor, double max_norm,
+                                       const double *rank_sumsq, int32_t nranks, void *stream);
 
 /* Norm and clip coefficient of the last step (fp64), and 1 if that norm was
  * not finite.  Any output pointer may be NULL.  Waits for the last step on

@@ -18,8 +18,8 @@ import ctypes
 from typing import Optional, Sequence
 
 from . import _abi
-from ._abi import (SOMA_DTYPE_BF16, SOMA_DTYPE_F32, SOMA_MAX_GROUPS, soma_plan_t,  # noqa: F401
-                   soma_tensor_t)
+from ._abi import (SOMA_DTYPE_BF16, SOMA_DTYPE_F16, SOMA_DTYPE_F32, SOMA_MAX_GROUPS,  # noqa: F401
+                   soma_plan_t, soma_tensor_t)
 
 __all__ = ["SomaOpt", "TensorList", "SomaError", "load", "soma_tensor_t", "soma_plan_t"]
 
@@ -40,7 +40,18 @@ def _grad_code(dtype) -> int:
         return SOMA_DTYPE_F32
     if dtype == torch.bfloat16:
         return SOMA_DTYPE_BF16
-    raise TypeError(f"unsupported gradient dtype {dtype} (float32 or bfloat16)")
+    if dtype == torch.float16:
+        return SOMA_DTYPE_F16
+    raise TypeError(f"unsupported gradient dtype {dtype} (float32, bfloat16 or float16)")
+
+
+def _lowp_code(dtype) -> int:
+    import torch
+    if dtype == torch.bfloat16:
+        return SOMA_DTYPE_BF16
+    if dtype == torch.float16:
+        return SOMA_DTYPE_F16
+    raise TypeError(f"unsupported model-weight dtype {dtype} (bfloat16 or float16)")
 
 
 def _stream_handle(stream) -> int:
@@ -52,24 +63,36 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
+def _check_f64_out(t, n):
+    import torch
+    if t.dtype != torch.float64 or not t.is_cuda or not t.is_contiguous() or t.numel() < n:
+        raise ValueError("expected a contiguous float64 CUDA tensor")
+
+
 class TensorList:
     """The soma_tensor_t array for lists of torch tensors, built once and
     reused every step (the tensors must stay alive and keep their storage).
 
     params / exp_avgs / exp_avg_sqs: contiguous float32 tensors.
-    grads: contiguous float32 or bfloat16 tensors (never written).
+    grads: contiguous float32, bfloat16 or float16 tensors (never written).
     groups: group id per tensor.  trainable / owned: bools per tensor
-    (default all True).  Frozen entries may pass None buffers."""
+    (default all True).  Frozen entries may pass None buffers.
+    params_lowp: optional bfloat16/float16 model weights per tensor (or None
+    entries), rewritten each step from the updated fp32 master `params`."""
 
     def __init__(self, params: Sequence, grads: Sequence, exp_avgs: Sequence, exp_avg_sqs: Sequence,
                  groups: Sequence[int], trainable: Optional[Sequence[bool]] = None,
-                 owned: Optional[Sequence[bool]] = None):
+                 owned: Optional[Sequence[bool]] = None, params_lowp: Optional[Sequence] = None):
         import torch
         n = len(params)
         if not (len(grads) == len(exp_avgs) == len(exp_avg_sqs) == len(groups) == n):
             raise ValueError("all per-tensor sequences must have the same length")
         trainable = [True] * n if trainable is None else list(trainable)
         owned = [True] * n if owned is None else list(owned)
+        params_lowp = [None] * n if params_lowp is None else list(params_lowp)
+        if len(params_lowp) != n:
+            raise ValueError("params_lowp must have one entry per tensor")
+        self.lowp = params_lowp  # keep alive
         self.n = n
         self.array = (soma_tensor_t * max(n, 1))()
         self.tensors = list(zip(params, grads, exp_avgs, exp_avg_sqs))  # keep alive
@@ -95,12 +118,16 @@ class TensorList:
             e.grad = ptr(g)
             e.exp_avg = ptr(m, torch.float32)
             e.exp_avg_sq = ptr(v, torch.float32)
+            lp = params_lowp[k]
+            if lp is not None and tr and lp.numel() != numel:
+                raise ValueError(f"tensor {k}: params_lowp must have the param's numel")
+            e.param_lowp = ptr(lp) if (lp is not None and tr) else None
+            e.lowp_dtype = _lowp_code(lp.dtype) if (lp is not None and tr) else 0
             e.numel = numel
             e.group = int(groups[k])
             e.grad_dtype = _grad_code(g.dtype) if (tr and g is not None) else 0
             e.trainable = 1 if tr else 0
             e.owned = 1 if owned[k] else 0
-            e.reserved = 0
 
     def pointer(self):
         return ctypes.cast(self.array, ctypes.POINTER(soma_tensor_t))
@@ -156,6 +183,22 @@ class SomaOpt:
     def step(self, tensors: TensorList, grad_divisor: float, max_norm: float, stream=None):
         self._check(_abi.soma_opt_step(self._h, tensors.pointer(), tensors.n, grad_divisor, max_norm,
                                        _stream_handle(stream)))
+
+    def sumsq(self, tensors: TensorList, grad_divisor: float, out, stream=None):
+        """This rank's sum of (g/d)^2 over owned entries into `out` (a float64
+        CUDA tensor with at least one element; written at out[0])."""
+        _check_f64_out(out, 1)
+        self._check(_abi.soma_opt_sumsq(self._h, tensors.pointer(), tensors.n, grad_divisor, out.data_ptr(),
+                                        _stream_handle(stream)))
+
+    def step_from_sumsq(self, tensors: TensorList, grad_divisor: float, max_norm: float, rank_sumsq,
+                        stream=None):
+        """The update with the global norm from all ranks' sums (a float64
+        CUDA tensor, rank r at index r)."""
+        _check_f64_out(rank_sumsq, 1)
+        self._check(_abi.soma_opt_step_from_sumsq(self._h, tensors.pointer(), tensors.n, grad_divisor, max_norm,
+                                                  rank_sumsq.data_ptr(), rank_sumsq.numel(),
+                                                  _stream_handle(stream)))
 
     def step_graph(self, tensors: TensorList, grad_divisor: float, max_norm: float, stream=None):
         """The graph-capturable step (soma_opt_step_graph): may be called

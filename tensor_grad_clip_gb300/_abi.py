@@ -22,8 +22,10 @@ SOMA_ERR_LIMIT = 8
 
 SOMA_DTYPE_F32 = 0
 SOMA_DTYPE_BF16 = 1
+SOMA_DTYPE_F16 = 2
 SOMA_MAX_GROUPS = 64
-SOMA_ABI_VERSION = 1
+SOMA_ABI_VERSION = 2
+SOMA_MAX_RANKS = 65536
 
 soma_status_t = ctypes.c_int32
 soma_opt_t = ctypes.c_void_p
@@ -35,16 +37,17 @@ class soma_tensor_t(ctypes.Structure):
         ("grad", ctypes.c_void_p),
         ("exp_avg", ctypes.c_void_p),
         ("exp_avg_sq", ctypes.c_void_p),
+        ("param_lowp", ctypes.c_void_p),
         ("numel", ctypes.c_int64),
         ("group", ctypes.c_int32),
         ("grad_dtype", ctypes.c_uint8),
         ("trainable", ctypes.c_uint8),
         ("owned", ctypes.c_uint8),
-        ("reserved", ctypes.c_uint8),
+        ("lowp_dtype", ctypes.c_uint8),
     ]
 
 
-assert ctypes.sizeof(soma_tensor_t) == 48
+assert ctypes.sizeof(soma_tensor_t) == 56
 
 
 class soma_plan_t(ctypes.Structure):
@@ -99,6 +102,10 @@ SIGNATURES = {
     "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),
     "soma_abi_version": (_I32, []),
     "soma_opt_destroy": (None, [soma_opt_t]),
+    "soma_opt_sumsq": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_tensor_t), _I64, _D, ctypes.c_void_p,
+                                       ctypes.c_void_p]),
+    "soma_opt_step_from_sumsq": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,
+                                                 ctypes.c_void_p, _I32, ctypes.c_void_p]),
     "soma_opt_step_graph": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,
                                             ctypes.c_void_p]),
     "soma_opt_push_groups": (soma_status_t, [soma_opt_t, ctypes.c_void_p]),

@@ -21,6 +21,8 @@
 //
 // Both kernels are HBM-bound streams (about 0.5 flop per byte); they use
 // 16-byte vector accesses and no tensor cores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -33,14 +35,51 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float bf16_one(uint16_t w) { return __uint_as_float((uint32_t)w << 16); }
+// fp16 widens through CUDA's conversion.
+__device__ __forceinline__ float2 f16_pair(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, sizeof h);
+    return __half22float2(h);
+}
+__device__ __forceinline__ float f16_one(uint16_t w) { return __half2float(__ushort_as_half(w)); }
 
-// Copy the chunk's segment descriptors into shared memory (3 x 16 B each).
+// Two consecutive 16-bit elements of a 32-bit word (the lower one first).
+template <int DT>
+__device__ __forceinline__ float2 pair16(uint32_t w) {
+    if (DT == kF16) return f16_pair(w);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+}
+template <int DT>
+__device__ __forceinline__ float one16(uint16_t w) {
+    return DT == kF16 ? f16_one(w) : bf16_one(w);
+}
+
+// Round two fp32 values to a packed pair of 16-bit values (nearest even).
+template <int LOW>
+__device__ __forceinline__ uint32_t pack16(float a, float b) {
+    uint32_t w;
+    if (LOW == kF16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        memcpy(&w, &h, sizeof w);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        memcpy(&w, &h, sizeof w);
+    }
+    return w;
+}
+template <int LOW>
+__device__ __forceinline__ uint16_t one_to16(float a) {
+    return LOW == kF16 ? __half_as_ushort(__float2half_rn(a)) : __bfloat16_as_ushort(__float2bfloat16_rn(a));
+}
+
+// Copy the chunk's segment descriptors into shared memory (4 x 16 B each).
 __device__ __forceinline__ int stage_segments(const Table& t, int chunk, Seg* sm) {
+    constexpr int kWords = sizeof(Seg) / sizeof(uint4);
     const int b = __ldg(t.chunk_begin + chunk);
     const int n = __ldg(t.chunk_begin + chunk + 1) - b;
     const uint4* src = reinterpret_cast<const uint4*>(t.segs + b);
     uint4* dst = reinterpret_cast<uint4*>(sm);
-    for (int i = threadIdx.x; i < 3 * n; i += blockDim.x) dst[i] = __ldg(src + i);
+    for (int i = threadIdx.x; i < kWords * n; i += blockDim.x) dst[i] = __ldg(src + i);
     __syncthreads();
     return n;
 }
@@ -79,16 +118,13 @@ __device__ __forceinline__ double block_sum64(double x, double* scratch) {
 
 // ---- square-sum of one segment, accumulated into a0 / a1 -----------------
 
-__device__ __forceinline__ void sq8_bf16(const uint4 w, float& a0, float& a1) {
-    float x;
-    x = bf16_lo(w.x); a0 = fmaf(x, x, a0);
-    x = bf16_hi(w.x); a1 = fmaf(x, x, a1);
-    x = bf16_lo(w.y); a0 = fmaf(x, x, a0);
-    x = bf16_hi(w.y); a1 = fmaf(x, x, a1);
-    x = bf16_lo(w.z); a0 = fmaf(x, x, a0);
-    x = bf16_hi(w.z); a1 = fmaf(x, x, a1);
-    x = bf16_lo(w.w); a0 = fmaf(x, x, a0);
-    x = bf16_hi(w.w); a1 = fmaf(x, x, a1);
+template <int DT>
+__device__ __forceinline__ void sq8_16(const uint4 w, float& a0, float& a1) {
+    float2 x;
+    x = pair16<DT>(w.x); a0 = fmaf(x.x, x.x, a0); a1 = fmaf(x.y, x.y, a1);
+    x = pair16<DT>(w.y); a0 = fmaf(x.x, x.x, a0); a1 = fmaf(x.y, x.y, a1);
+    x = pair16<DT>(w.z); a0 = fmaf(x.x, x.x, a0); a1 = fmaf(x.y, x.y, a1);
+    x = pair16<DT>(w.w); a0 = fmaf(x.x, x.x, a0); a1 = fmaf(x.y, x.y, a1);
 }
 
 __device__ __forceinline__ void sq4_f32(const float4 u, float& a0, float& a1) {
@@ -96,10 +132,11 @@ __device__ __forceinline__ void sq4_f32(const float4 u, float& a0, float& a1) {
     a0 = fmaf(u.z, u.z, a0); a1 = fmaf(u.w, u.w, a1);
 }
 
-__device__ __forceinline__ void sumsq_bf16(const Seg& s, float& a0, float& a1) {
+template <int DT>
+__device__ __forceinline__ void sumsq_16(const Seg& s, float& a0, float& a1) {
     const uint16_t* g = static_cast<const uint16_t*>(s.g);
     for (int j = threadIdx.x; j < s.head; j += blockDim.x) {
-        float x = bf16_one(__ldg(g + j));
+        float x = one16<DT>(__ldg(g + j));
         a0 = fmaf(x, x, a0);
     }
     const uint4* gv = reinterpret_cast<const uint4*>(g + s.head);
@@ -108,14 +145,14 @@ __device__ __forceinline__ void sumsq_bf16(const Seg& s, float& a0, float& a1) {
     for (; i + 3 * S < s.nvec; i += 4 * S) {  // four independent 16-byte loads in flight
         const uint4 w0 = __ldg(gv + i), w1 = __ldg(gv + i + S);
         const uint4 w2 = __ldg(gv + i + 2 * S), w3 = __ldg(gv + i + 3 * S);
-        sq8_bf16(w0, a0, a1);
-        sq8_bf16(w1, a0, a1);
-        sq8_bf16(w2, a0, a1);
-        sq8_bf16(w3, a0, a1);
+        sq8_16<DT>(w0, a0, a1);
+        sq8_16<DT>(w1, a0, a1);
+        sq8_16<DT>(w2, a0, a1);
+        sq8_16<DT>(w3, a0, a1);
     }
-    for (; i < s.nvec; i += S) sq8_bf16(__ldg(gv + i), a0, a1);
+    for (; i < s.nvec; i += S) sq8_16<DT>(__ldg(gv + i), a0, a1);
     for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
-        float x = bf16_one(__ldg(g + j));
+        float x = one16<DT>(__ldg(g + j));
         a1 = fmaf(x, x, a1);
     }
 }
@@ -175,7 +212,8 @@ __global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant_
         const int ns = stage_segments(a.t, c, segs);
         float a0 = 0.f, a1 = 0.f;
         for (int s = 0; s < ns; ++s) {
-            if (segs[s].gdtype == kBF16) sumsq_bf16(segs[s], a0, a1);
+            if (segs[s].gdtype == kBF16) sumsq_16<kBF16>(segs[s], a0, a1);
+            else if (segs[s].gdtype == kF16) sumsq_16<kF16>(segs[s], a0, a1);
             else sumsq_f32(segs[s], a0, a1);
         }
         const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
@@ -217,6 +255,7 @@ __global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant_
         a.res->scale = (float)(coef / a.divisor);
         a.res->nonfinite = isfinite(norm) ? 0u : 1u;
         a.res->ticket = 0u;
+        if (a.sumsq_out) *a.sumsq_out = s / (a.divisor * a.divisor);
     }
     if (kGraph) {
         const int q = threadIdx.x;
@@ -226,6 +265,22 @@ __global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant_
             a.dhp[q] = group_constants(a.dgroups[q], t);
         }
     }
+}
+
+// Multi-rank step: the global norm from the ranks' square-sums, added in
+// rank order so every rank derives the same bits.
+__global__ void finish_kernel(const __grid_constant__ FinishArgs a) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    double s = 0.0;
+    for (int r = 0; r < a.count; ++r) s += a.parts[r];
+    const double norm = sqrt(s);
+    const double q = a.max_norm / (norm + 1e-6);
+    const double coef = (q < 1.0 || q != q) ? q : 1.0;
+    a.res->sumsq = s;
+    a.res->norm = norm;
+    a.res->coef = coef;
+    a.res->scale = (float)(coef / a.divisor);
+    a.res->nonfinite = isfinite(norm) ? 0u : 1u;
 }
 
 // ---- fused update --------------------------------------------------------
@@ -238,17 +293,20 @@ __device__ __forceinline__ void adamw(float& p, float& m, float& v, float g, con
     p = fmaf(-h.step_size, m / denom, p);
 }
 
+template <int DT>
 __device__ __forceinline__ float grad_one(const Seg& s, int j) {
-    return s.gdtype == kBF16 ? bf16_one(__ldcs(static_cast<const unsigned short*>(s.g) + j))
-                             : __ldcs(static_cast<const float*>(s.g) + j);
+    if (DT == kF32) return __ldcs(static_cast<const float*>(s.g) + j);
+    return one16<DT>(__ldcs(static_cast<const unsigned short*>(s.g) + j));
 }
 
+template <int DT, int LOW>
 __device__ __forceinline__ void update_one(const Seg& s, int j, const GroupHp& h, float scale) {
     float p = __ldcs(s.p + j), m = __ldcs(s.m + j), v = __ldcs(s.v + j);
-    adamw(p, m, v, grad_one(s, j) * scale, h);
+    adamw(p, m, v, grad_one<DT>(s, j) * scale, h);
     __stcs(s.p + j, p);
     __stcs(s.m + j, m);
     __stcs(s.v + j, v);
+    if (LOW != kNone) __stcs(static_cast<unsigned short*>(s.plow) + j, one_to16<LOW>(p));
 }
 
 struct Lane8 {
@@ -261,18 +319,19 @@ __device__ __forceinline__ void load8(const Seg& s, int i, Lane8& x) {
     const float4* p = reinterpret_cast<const float4*>(s.p + s.head) + 2 * i;
     const float4* m = reinterpret_cast<const float4*>(s.m + s.head) + 2 * i;
     const float4* v = reinterpret_cast<const float4*>(s.v + s.head) + 2 * i;
-    if (DT == kBF16) {
-        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(
-                                   static_cast<const uint16_t*>(s.g) + s.head) + i);
-        x.g[0] = bf16_lo(w.x); x.g[1] = bf16_hi(w.x);
-        x.g[2] = bf16_lo(w.y); x.g[3] = bf16_hi(w.y);
-        x.g[4] = bf16_lo(w.z); x.g[5] = bf16_hi(w.z);
-        x.g[6] = bf16_lo(w.w); x.g[7] = bf16_hi(w.w);
-    } else {
+    if (DT == kF32) {
         const float4* g = reinterpret_cast<const float4*>(static_cast<const float*>(s.g) + s.head) + 2 * i;
         const float4 u = __ldcs(g), w = __ldcs(g + 1);
         x.g[0] = u.x; x.g[1] = u.y; x.g[2] = u.z; x.g[3] = u.w;
         x.g[4] = w.x; x.g[5] = w.y; x.g[6] = w.z; x.g[7] = w.w;
+    } else {
+        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(
+                                   static_cast<const uint16_t*>(s.g) + s.head) + i);
+        float2 t;
+        t = pair16<DT>(w.x); x.g[0] = t.x; x.g[1] = t.y;
+        t = pair16<DT>(w.y); x.g[2] = t.x; x.g[3] = t.y;
+        t = pair16<DT>(w.z); x.g[4] = t.x; x.g[5] = t.y;
+        t = pair16<DT>(w.w); x.g[6] = t.x; x.g[7] = t.y;
     }
     x.p0 = __ldcs(p); x.p1 = __ldcs(p + 1);
     x.m0 = __ldcs(m); x.m1 = __ldcs(m + 1);
@@ -290,6 +349,7 @@ __device__ __forceinline__ void compute8(Lane8& x, const GroupHp& h, float scale
     adamw(x.p1.w, x.m1.w, x.v1.w, x.g[7] * scale, h);
 }
 
+template <int LOW>
 __device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
     float4* p = reinterpret_cast<float4*>(s.p + s.head) + 2 * i;
     float4* m = reinterpret_cast<float4*>(s.m + s.head) + 2 * i;
@@ -297,10 +357,19 @@ __device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
     __stcs(p, x.p0); __stcs(p + 1, x.p1);
     __stcs(m, x.m0); __stcs(m + 1, x.m1);
     __stcs(v, x.v0); __stcs(v + 1, x.v1);
+    if (LOW != kNone) {
+        uint4 w;
+        w.x = pack16<LOW>(x.p0.x, x.p0.y);
+        w.y = pack16<LOW>(x.p0.z, x.p0.w);
+        w.z = pack16<LOW>(x.p1.x, x.p1.y);
+        w.w = pack16<LOW>(x.p1.z, x.p1.w);
+        __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.plow) + s.head) + i, w);
+    }
 }
 
-template <int DT>
-__device__ __forceinline__ void update_body(const Seg& s, const GroupHp& h, float scale) {
+template <int DT, int LOW>
+__device__ __forceinline__ void update_segment(const Seg& s, const GroupHp& h, float scale) {
+    for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one<DT, LOW>(s, j, h, scale);
     const int n = s.nvec;
     const int stride = blockDim.x;
     int i = threadIdx.x;
@@ -310,15 +379,24 @@ __device__ __forceinline__ void update_body(const Seg& s, const GroupHp& h, floa
         load8<DT>(s, i + stride, x1);
         compute8(x0, h, scale);
         compute8(x1, h, scale);
-        store8(s, i, x0);
-        store8(s, i + stride, x1);
+        store8<LOW>(s, i, x0);
+        store8<LOW>(s, i + stride, x1);
     }
     if (i < n) {
         Lane8 x0;
         load8<DT>(s, i, x0);
         compute8(x0, h, scale);
-        store8(s, i, x0);
+        store8<LOW>(s, i, x0);
     }
+    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x)
+        update_one<DT, LOW>(s, j, h, scale);
+}
+
+template <int DT>
+__device__ __forceinline__ void update_segment_low(const Seg& s, const GroupHp& h, float scale) {
+    if (s.lowdt == kBF16) update_segment<DT, kBF16>(s, h, scale);
+    else if (s.lowdt == kF16) update_segment<DT, kF16>(s, h, scale);
+    else update_segment<DT, kNone>(s, h, scale);
 }
 
 // Chunks run in reverse list order: the gradients the square-sum kernel read
@@ -337,11 +415,9 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
         for (int k = 0; k < ns; ++k) {
             const Seg& s = segs[k];
             const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
-            for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one(s, j, h, scale);
-            if (s.gdtype == kBF16) update_body<kBF16>(s, h, scale);
-            else update_body<kF32>(s, h, scale);
-            for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x)
-                update_one(s, j, h, scale);
+            if (s.gdtype == kBF16) update_segment_low<kBF16>(s, h, scale);
+            else if (s.gdtype == kF16) update_segment_low<kF16>(s, h, scale);
+            else update_segment_low<kF32>(s, h, scale);
         }
         __syncthreads();  // segs is restaged for the next chunk
     }
@@ -358,6 +434,11 @@ int launch_norm(const NormArgs& a, int grid, void* stream, bool graph) {
 int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph) {
     if (graph) update_kernel<true><<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
     else update_kernel<false><<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_finish(const FinishArgs& a, void* stream) {
+    finish_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return (int)cudaGetLastError();
 }
 

@@ -64,7 +64,7 @@ void norm_table(const soma_tensor_t* list, int64_t n, int64_t chunk, soma::Seg* 
     for (int64_t k = 0; k < n; ++k) {
         const soma_tensor_t& t = list[k];
         if (!t.trainable || !t.owned || t.numel == 0) continue;
-        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
+        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;  // fp32, or bf16 / fp16
         int h = -1;
         for (int c = 0; c < soma::kVec && h < 0; ++c)
             if (((uintptr_t)t.grad + (uintptr_t)c * gsz) % 16 == 0) h = c;
@@ -136,9 +136,10 @@ extern "C" soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tenso
     int64_t owned = 0;
     for (int64_t k = 0; k < n; ++k) {
         const soma_tensor_t& t = list[k];
-        if (t.reserved != 0 || t.trainable > 1 || t.owned > 1 || t.numel < 0) return SOMA_ERR_INVALID_ARG;
+        if (t.trainable > 1 || t.owned > 1 || t.numel < 0) return SOMA_ERR_INVALID_ARG;
         if (!t.trainable || !t.owned || t.numel == 0) continue;
-        if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16) return SOMA_ERR_DTYPE;
+        if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16 && t.grad_dtype != SOMA_DTYPE_F16)
+            return SOMA_ERR_DTYPE;
         if (!t.grad) return SOMA_ERR_INVALID_ARG;
         if ((uintptr_t)t.grad % (t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2)) return SOMA_ERR_ALIGNMENT;
         owned += t.numel;

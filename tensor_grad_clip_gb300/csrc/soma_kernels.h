@@ -28,21 +28,23 @@ constexpr int kVec = 8;                 // elements per vector step
 constexpr int kMaxSegsPerChunk = 64;    // bounds the shared-memory segment cache
 constexpr int kMaxGroups = 64;
 
-enum : int32_t { kF32 = 0, kBF16 = 1 };
+enum : int32_t { kNone = 0, kF32 = 0, kBF16 = 1, kF16 = 2 };
 
-struct Seg {                // 48 bytes
+struct Seg {                // 64 bytes
     float* p;               // already offset to the segment's first element
     const void* g;
     float* m;
     float* v;
+    void* plow;             // bf16/fp16 copy of p written by the update, or nullptr
     int32_t len;            // elements in the segment
     int32_t head;           // scalar elements before the vector body
     int32_t nvec;           // 8-element vectors in the body
     uint16_t group;
-    uint8_t gdtype;
-    uint8_t pad;
+    uint8_t gdtype;         // kF32, kBF16, kF16
+    uint8_t lowdt;          // kNone, kBF16, kF16
+    uint64_t pad;
 };
-static_assert(sizeof(Seg) == 48, "Seg layout");
+static_assert(sizeof(Seg) == 64, "Seg layout");
 
 // Per-group constants of one step, derived on the host in fp64 and rounded
 // once to fp32.
@@ -95,6 +97,19 @@ struct NormArgs {
     GroupHp* dhp;
     uint64_t present;
     int32_t ngroups;
+    // multi-rank step: when set, the last CTA also stores this rank's
+    // normalized square-sum S / d^2 here
+    double* sumsq_out;
+};
+
+// Multi-rank step: one thread adds the ranks' normalized square-sums in rank
+// order and derives norm, c and the update scale.
+struct FinishArgs {
+    const double* parts;
+    int32_t count;
+    Result* res;
+    double divisor;
+    double max_norm;
 };
 
 struct UpdateArgs {
@@ -113,5 +128,6 @@ constexpr int kUpdateBlock = 256;
 // memory (NormArgs::dgroups / dhp, UpdateArgs::dhp).
 int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false);
 int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false);
+int launch_finish(const FinishArgs& a, void* stream);
 
 }  // namespace soma

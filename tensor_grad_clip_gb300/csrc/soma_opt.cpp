@@ -138,8 +138,9 @@ soma_status_t check_group_hp(soma_opt* o, double lr, double b1, double b2, doubl
     return SOMA_OK;
 }
 
+int grad_size(uint8_t dtype) { return dtype == SOMA_DTYPE_F32 ? 4 : 2; }
+
 soma_status_t validate_entry(soma_opt* o, const soma_tensor_t& t, int64_t k) {
-    if (t.reserved != 0) return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld].reserved must be 0", (long long)k);
     if (t.trainable > 1 || t.owned > 1)
         return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld]: trainable and owned must be 0 or 1", (long long)k);
     if (t.numel < 0) return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld].numel < 0", (long long)k);
@@ -147,14 +148,16 @@ soma_status_t validate_entry(soma_opt* o, const soma_tensor_t& t, int64_t k) {
     if (t.group < 0 || t.group >= (int32_t)o->groups.size())
         return o->fail(SOMA_ERR_BAD_GROUP, "list[%lld].group = %d, have %zu groups", (long long)k, t.group,
                        o->groups.size());
-    if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16)
+    if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16 && t.grad_dtype != SOMA_DTYPE_F16)
         return o->fail(SOMA_ERR_DTYPE, "list[%lld].grad_dtype = %d", (long long)k, (int)t.grad_dtype);
+    if (t.param_lowp ? (t.lowp_dtype != SOMA_DTYPE_BF16 && t.lowp_dtype != SOMA_DTYPE_F16) : t.lowp_dtype != 0)
+        return o->fail(SOMA_ERR_DTYPE, "list[%lld]: lowp_dtype = %d does not match param_lowp", (long long)k,
+                       (int)t.lowp_dtype);
     if (t.numel == 0) return SOMA_OK;
     if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq)
         return o->fail(SOMA_ERR_INVALID_ARG, "list[%lld]: null buffer in a trainable entry", (long long)k);
-    const uintptr_t ge = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
     if ((uintptr_t)t.param % 4 || (uintptr_t)t.exp_avg % 4 || (uintptr_t)t.exp_avg_sq % 4 ||
-        (uintptr_t)t.grad % ge)
+        (uintptr_t)t.grad % grad_size(t.grad_dtype) || (uintptr_t)t.param_lowp % 2)
         return o->fail(SOMA_ERR_ALIGNMENT, "list[%lld]: a buffer is not aligned to its element size",
                        (long long)k);
     return SOMA_OK;
@@ -191,7 +194,7 @@ struct TableBuilder {
     // h: vector head of the tensor, -1 = process every element singly.
     void add(const soma_tensor_t& t, int h, bool with_state) {
         const int64_t n = t.numel;
-        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
+        const int gsz = grad_size(t.grad_dtype);
         int64_t off = 0;
         while (off < n) {
             if (cur_segs == soma::kMaxSegsPerChunk || cur_elems >= chunk) close();
@@ -206,6 +209,8 @@ struct TableBuilder {
             s.m = with_state ? t.exp_avg + off : nullptr;
             s.v = with_state ? t.exp_avg_sq + off : nullptr;
             s.g = static_cast<const char*>(t.grad) + off * gsz;
+            s.plow = (with_state && t.param_lowp) ? static_cast<char*>(t.param_lowp) + off * 2 : nullptr;
+            s.lowdt = (with_state && t.param_lowp) ? t.lowp_dtype : 0;
             s.len = (int32_t)len;
             if (h < 0) {
                 s.head = (int32_t)len;
@@ -283,14 +288,13 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
         if (!t.trainable) continue;
         present[t.group] = 1;
         if (t.numel == 0) continue;
-        const int gsz = t.grad_dtype == SOMA_DTYPE_F32 ? 4 : 2;
-        const uintptr_t a4[4] = {(uintptr_t)t.grad, (uintptr_t)t.param, (uintptr_t)t.exp_avg,
-                                 (uintptr_t)t.exp_avg_sq};
-        const int e4[4] = {gsz, 4, 4, 4};
-        upd.add(t, vector_head(a4, e4, 4), true);
+        const uintptr_t a5[5] = {(uintptr_t)t.grad, (uintptr_t)t.param, (uintptr_t)t.exp_avg,
+                                 (uintptr_t)t.exp_avg_sq, (uintptr_t)t.param_lowp};
+        const int e5[5] = {grad_size(t.grad_dtype), 4, 4, 4, 2};
+        upd.add(t, vector_head(a5, e5, t.param_lowp ? 5 : 4), true);
         trainable += t.numel;
         if (t.owned) {
-            nrm.add(t, vector_head(a4, e4, 1), false);
+            nrm.add(t, vector_head(a5, e5, 1), false);
             owned += t.numel;
         }
     }
@@ -550,19 +554,11 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
     return SOMA_OK;
 }
 
-soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,
-                            double max_norm, void* stream) {
-    soma_opt* o = live_handle(h);
-    if (!o) return SOMA_ERR_STATE;
-    // An unchanged list was validated when it was cached (groups are never removed).
-    bool same = false;
-    soma_status_t st0 = check_step_args(o, list, n, grad_divisor, max_norm, &same);
-    if (st0 != SOMA_OK) return st0;
-    if (!same && o->graph_locked)
-        return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
+namespace {
 
-    DeviceGuard dg(o->device);
-    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+// Everything a step does before its launches, after the arguments were
+// checked: device, ordering after the previous step, tables for this list.
+soma_status_t prepare(soma_opt* o, const soma_tensor_t* list, int64_t n, bool same, void* stream) {
     soma_status_t st = ensure_device(o);
     if (st != SOMA_OK) return st;
     cudaError_t e;
@@ -575,12 +571,13 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
         o->cache_valid = false;
         if ((st = rebuild(o, list, n, stream)) != SOMA_OK) return st;
     }
+    return SOMA_OK;
+}
 
-    // Per-group constants for this step (fp64 on the host, rounded once).
-    soma::UpdateArgs ua{};
-    ua.t = o->upd_tab;
-    ua.res = o->d_res;
-    std::vector<int64_t> next(o->groups.size());
+// Per-group constants of the next step (fp64 on the host, rounded once) and
+// the step counts it will reach.
+void host_group_constants(soma_opt* o, soma::UpdateArgs& ua, std::vector<int64_t>& next) {
+    next.assign(o->groups.size(), 0);
     for (size_t q = 0; q < o->groups.size(); ++q) {
         const Group& g = o->groups[q];
         const bool on = q < o->group_present.size() && o->group_present[q];
@@ -599,13 +596,19 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
         hp.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
         hp.eps = (float)g.eps;
     }
-    soma::NormArgs na{};
-    na.t = o->norm_tab;
-    na.partials = o->d_partials;
-    na.res = o->d_res;
-    na.divisor = grad_divisor;
-    na.max_norm = max_norm;
+}
 
+// The launches of a step: the norm side (the square-sum kernel, or for the
+// multi-rank step the finish kernel over the ranks' sums), then the update.
+soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, const double* rank_sums,
+                          int32_t nranks, void* stream) {
+    soma::UpdateArgs ua{};
+    ua.t = o->upd_tab;
+    ua.res = o->d_res;
+    std::vector<int64_t> next;
+    host_group_constants(o, ua, next);
+    cudaError_t e;
+    soma_status_t st;
     std::array<cudaEvent_t, 3>* ev = nullptr;
     if (o->timing) {
         if (o->tev_used == kTimingRing && (st = timing_flush(o)) != SOMA_OK) return st;
@@ -619,8 +622,20 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
         if ((e = cudaEventRecord((*ev)[0], (cudaStream_t)stream)) != cudaSuccess)
             return o->cuda_fail(e, "cudaEventRecord");
     }
-    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream)) != cudaSuccess)
-        return o->cuda_fail(e, "launching the square-sum kernel");
+    if (rank_sums) {
+        soma::FinishArgs fa{rank_sums, nranks, o->d_res, grad_divisor, max_norm};
+        if ((e = (cudaError_t)soma::launch_finish(fa, stream)) != cudaSuccess)
+            return o->cuda_fail(e, "launching the finish kernel");
+    } else {
+        soma::NormArgs na{};
+        na.t = o->norm_tab;
+        na.partials = o->d_partials;
+        na.res = o->d_res;
+        na.divisor = grad_divisor;
+        na.max_norm = max_norm;
+        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream)) != cudaSuccess)
+            return o->cuda_fail(e, "launching the square-sum kernel");
+    }
     if (ev && (e = cudaEventRecord((*ev)[1], (cudaStream_t)stream)) != cudaSuccess)
         return o->cuda_fail(e, "cudaEventRecord");
     if (o->upd_grid > 0 && (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream)) != cudaSuccess)
@@ -639,6 +654,75 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
         o->groups[q].step = next[q];
     }
     return SOMA_OK;
+}
+
+}  // namespace
+
+soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,
+                            double max_norm, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    // An unchanged list was validated when it was cached (groups are never removed).
+    bool same = false;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    if (st != SOMA_OK) return st;
+    if (!same && o->graph_locked)
+        return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    if ((st = prepare(o, list, n, same, stream)) != SOMA_OK) return st;
+    return launch_step(o, grad_divisor, max_norm, nullptr, 0, stream);
+}
+
+soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,
+                             double* sumsq_out, void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!sumsq_out || (uintptr_t)sumsq_out % alignof(double) != 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "sumsq_out must be a non-null, 8-byte aligned device pointer");
+    bool same = false;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, 1.0, &same);
+    if (st != SOMA_OK) return st;
+    if (!same && o->graph_locked)
+        return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    if ((st = prepare(o, list, n, same, stream)) != SOMA_OK) return st;
+    soma::NormArgs na{};
+    na.t = o->norm_tab;
+    na.partials = o->d_partials;
+    na.res = o->d_res;
+    na.divisor = grad_divisor;
+    na.max_norm = 1.0;
+    na.sumsq_out = sumsq_out;
+    cudaError_t e;
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream)) != cudaSuccess)
+        return o->cuda_fail(e, "launching the square-sum kernel");
+    if ((e = cudaEventRecord(o->done, (cudaStream_t)stream)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaEventRecord");
+    o->have_done = true;
+    o->last_stream = stream;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_step_from_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,
+                                       double max_norm, const double* rank_sumsq, int32_t nranks,
+                                       void* stream) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (!rank_sumsq || (uintptr_t)rank_sumsq % alignof(double) != 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "rank_sumsq must be a non-null, 8-byte aligned device pointer");
+    if (nranks < 1 || nranks > SOMA_MAX_RANKS)
+        return o->fail(SOMA_ERR_INVALID_ARG, "nranks must be in [1, %d]", SOMA_MAX_RANKS);
+    bool same = false;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    if (st != SOMA_OK) return st;
+    if (!same && o->graph_locked)
+        return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    if ((st = prepare(o, list, n, same, stream)) != SOMA_OK) return st;
+    return launch_step(o, grad_divisor, max_norm, rank_sumsq, nranks, stream);
 }
 
 soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64_t n, double grad_divisor,

@@ -51,12 +51,18 @@ class DeviceList:
         self.w = w
         self.device = device
         self.bufs = []      # (full buffer, sentinel word, view slice)
-        self.p, self.g, self.m, self.v = [], [], [], []
+        self.p, self.g, self.m, self.v, self.plow = [], [], [], [], []
         for k, t in enumerate(w.tensors):
             sp, sg, sm, sv = shift[k] if shift is not None else (0, 0, 0, 0)
             gdt = W.torch_dtype(t.grad_dtype)
             p = self._alloc(t.numel, torch.float32, sp)
             p.copy_(params_cpu[k].reshape(-1).to(device))
+            if t.param_lowp:
+                lp = self._alloc(t.numel, W.torch_dtype(t.param_lowp), sp)
+                lp.copy_(p.to(lp.dtype))
+                self.plow.append(lp)
+            else:
+                self.plow.append(None)
             g = self._alloc(t.numel, gdt, sg)
             m = self._alloc(t.numel, torch.float32, sm)
             v = self._alloc(t.numel, torch.float32, sv)
@@ -71,10 +77,11 @@ class DeviceList:
             none = lambda xs: [x if tr else None for x, tr in zip(xs, trainable)]
             self.tl = TensorList(self.p, none(self.g), none(self.m), none(self.v),
                                  groups=[t.group for t in w.tensors], trainable=trainable,
-                                 owned=[t.owned for t in w.tensors])
+                                 owned=[t.owned for t in w.tensors], params_lowp=self.plow)
         else:
             self.tl = TensorList(self.p, self.g, self.m, self.v, groups=[t.group for t in w.tensors],
-                                 trainable=trainable, owned=[t.owned for t in w.tensors])
+                                 trainable=trainable, owned=[t.owned for t in w.tensors],
+                                 params_lowp=self.plow)
 
     def _alloc(self, numel, dtype, shift):
         full = torch.empty(numel + 2 * PAD + 8, dtype=dtype, device=self.device)
@@ -100,17 +107,33 @@ class DeviceList:
         snap = {"g": [x.clone() for x in self.g]}
         snap["frozen"] = [(k, self.p[k].clone(), self.m[k].clone(), self.v[k].clone())
                           for k, t in enumerate(self.w.tensors) if not t.trainable]
+        snap["frozen_lowp"] = [(k, self.plow[k].clone()) for k, t in enumerate(self.w.tensors)
+                               if not t.trainable and self.plow[k] is not None]
         return snap
 
+    def check_lowp_copies(self):
+        """Each model copy is the round-to-nearest-even image of the fp32
+        weights the kernel just wrote (torch's CPU conversion as reference)."""
+        for k, t in enumerate(self.w.tensors):
+            lp = self.plow[k]
+            if lp is None or not t.trainable:
+                continue
+            ref = self.p[k].cpu().to(lp.dtype)
+            if not torch.equal(lp.cpu().view(torch.int16), ref.view(torch.int16)):
+                raise AssertionError(f"tensor {k}: {lp.dtype} copy is not the rounded fp32 weights")
+
     def check_snapshot(self, snap):
+        bits = lambda x: x.view(torch.int16) if x.element_size() == 2 else x.view(torch.int32)
         for k, (a, b) in enumerate(zip(snap["g"], self.g)):
-            if not torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
-                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)):
+            if not torch.equal(bits(a), bits(b)):
                 raise AssertionError(f"gradient {k} changed")
         for k, p, m, v in snap["frozen"]:
             for x, y in ((p, self.p[k]), (m, self.m[k]), (v, self.v[k])):
                 if not torch.equal(x.view(torch.int32), y.view(torch.int32)):
                     raise AssertionError(f"frozen tensor {k} changed")
+        for k, lp in snap.get("frozen_lowp", []):
+            if not torch.equal(lp.view(torch.int16), self.plow[k].view(torch.int16)):
+                raise AssertionError(f"frozen tensor {k}'s model copy changed")
 
 
 def make_opt(w: W.Workload, device_index=0) -> SomaOpt:
@@ -158,6 +181,7 @@ def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=
             assert coef == 1.0
         dl.check_snapshot(snap)
         dl.check_guards()
+        dl.check_lowp_copies()
         if check_every_step or s == steps:
             for k, t in enumerate(w.tensors):
                 if not t.trainable:

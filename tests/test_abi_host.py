@@ -36,9 +36,10 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_layout():
-    assert ctypes.sizeof(_abi.soma_tensor_t) == 48
-    assert _abi.soma_tensor_t.numel.offset == 32 and _abi.soma_tensor_t.group.offset == 40
-    assert _abi.soma_tensor_t.reserved.offset == 47
+    assert ctypes.sizeof(_abi.soma_tensor_t) == 56
+    assert _abi.soma_tensor_t.param_lowp.offset == 32
+    assert _abi.soma_tensor_t.numel.offset == 40 and _abi.soma_tensor_t.group.offset == 48
+    assert _abi.soma_tensor_t.lowp_dtype.offset == 55
 
 
 def test_status_strings(lib):
@@ -93,7 +94,8 @@ def test_group_limit():
 def _entry(**kw):
     e = _abi.soma_tensor_t()
     e.param, e.grad, e.exp_avg, e.exp_avg_sq = 0x10000, 0x20000, 0x30000, 0x40000
-    e.numel, e.group, e.grad_dtype, e.trainable, e.owned, e.reserved = 8, 0, 0, 1, 1, 0
+    e.param_lowp = 0
+    e.numel, e.group, e.grad_dtype, e.trainable, e.owned, e.lowp_dtype = 8, 0, 0, 1, 1, 0
     for k, v in kw.items():
         setattr(e, k, v)
     return e
@@ -105,7 +107,11 @@ def _step(opt, entries, divisor=1.0, max_norm=1.0, n=None):
 
 
 @pytest.mark.parametrize("entry,status", [
-    (dict(reserved=1), _abi.SOMA_ERR_INVALID_ARG),
+    (dict(lowp_dtype=1), _abi.SOMA_ERR_DTYPE),                      # dtype without a copy
+    (dict(param_lowp=0x50000), _abi.SOMA_ERR_DTYPE),                # copy without a dtype
+    (dict(param_lowp=0x50000, lowp_dtype=3), _abi.SOMA_ERR_DTYPE),
+    (dict(param_lowp=0x50001, lowp_dtype=1), _abi.SOMA_ERR_ALIGNMENT),
+    (dict(grad=0x20001, grad_dtype=2), _abi.SOMA_ERR_ALIGNMENT),    # fp16 grad on an odd address
     (dict(trainable=2), _abi.SOMA_ERR_INVALID_ARG),
     (dict(owned=3), _abi.SOMA_ERR_INVALID_ARG),
     (dict(numel=-1), _abi.SOMA_ERR_INVALID_ARG),
@@ -204,9 +210,43 @@ def test_tensor_list_marshalling_checks():
     with pytest.raises(ValueError):
         TensorList([p.t()], [g], [p], [p], groups=[0])  # non-contiguous
     with pytest.raises(TypeError):
-        TensorList([p], [g.half()], [p], [p], groups=[0])
+        TensorList([p], [g.double()], [p], [p], groups=[0])
+    with pytest.raises(TypeError):
+        TensorList([p], [g], [p], [p], groups=[0], params_lowp=[p])  # fp32 is not a 16-bit copy
+    tl16 = TensorList([p], [g.half()], [p], [p], groups=[0], params_lowp=[g])
+    assert tl16.array[0].grad_dtype == _abi.SOMA_DTYPE_F16 and tl16.array[0].lowp_dtype == _abi.SOMA_DTYPE_BF16
     with pytest.raises(ValueError):
         TensorList([p], [torch.zeros(3)], [p], [p], groups=[0])
     tl = TensorList([p, p], [g, None], [p, None], [p, None], groups=[0, 0], trainable=[True, False])
     assert tl.array[0].grad_dtype == _abi.SOMA_DTYPE_BF16 and tl.array[1].trainable == 0
     assert tl.array[1].grad is None and tl.array[0].numel == 16
+
+
+def test_multirank_entry_points_reject_bad_arguments():
+    opt = SomaOpt(0)
+    opt.add_group(lr=1e-3)
+    arr = (_abi.soma_tensor_t * 1)(_entry())
+    h = opt.handle
+    assert _abi.soma_opt_sumsq(h, arr, 1, 1.0, None, None) == _abi.SOMA_ERR_INVALID_ARG
+    assert _abi.soma_opt_sumsq(h, arr, 1, 1.0, 0x1004, None) == _abi.SOMA_ERR_INVALID_ARG  # not 8-byte aligned
+    assert _abi.soma_opt_sumsq(h, arr, 1, 0.0, 0x1000, None) == _abi.SOMA_ERR_INVALID_ARG  # divisor
+    f = _abi.soma_opt_step_from_sumsq
+    assert f(h, arr, 1, 1.0, 1.0, None, 1, None) == _abi.SOMA_ERR_INVALID_ARG
+    assert f(h, arr, 1, 1.0, 1.0, 0x1000, 0, None) == _abi.SOMA_ERR_INVALID_ARG
+    assert f(h, arr, 1, 1.0, 1.0, 0x1000, _abi.SOMA_MAX_RANKS + 1, None) == _abi.SOMA_ERR_INVALID_ARG
+    bad = (_abi.soma_tensor_t * 1)(_entry(group=4))
+    assert f(h, bad, 1, 1.0, 1.0, 0x1000, 2, None) == _abi.SOMA_ERR_BAD_GROUP
+    assert opt.get_group_step(0) == 0
+    opt.close()
+
+
+def test_owned_flags_count_every_entry_once():
+    from tensor_grad_clip_gb300.sharded import owned_flags
+    sharded = [True, False, False, True, False]
+    world = 3
+    flags = [owned_flags(5, r, world, sharded) for r in range(world)]
+    for k in range(5):
+        owners = [r for r in range(world) if flags[r][k]]
+        assert owners == (list(range(world)) if sharded[k] else [k % world])
+    with pytest.raises(ValueError):
+        owned_flags(5, 3, 3, sharded)

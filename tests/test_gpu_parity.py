@@ -261,3 +261,20 @@ def test_timing_counts_steps():
     assert n == 3 and a > 0 and b > 0
     assert opt.read_timing() == (0.0, 0.0, 0)
     opt.close()
+
+
+@pytest.mark.parametrize("grad_dt,low_dt", [(W.F16, None), (W.BF16, W.BF16), (W.F16, W.F16), (W.F32, W.BF16),
+                                            (W.BF16, W.F16)])
+def test_fp16_grads_and_master_weight_copies(grad_dt, low_dt):
+    # fp16 gradients, and bf16/fp16 model weights rewritten from the fp32
+    # master copy in the same pass (the RLinf page's FP32MasterAdamW): the
+    # master weights follow the oracle, each copy is its exact rounding.
+    T = W.TensorSpec
+    tensors = [T("a", (96, 80), grad_dt, param_lowp=low_dt), T("b", (80,), grad_dt, group=1, param_lowp=low_dt),
+               T("c", (5003,), grad_dt, param_lowp=low_dt, owned=False), T("d", (7,), grad_dt, param_lowp=low_dt),
+               T("e", (70001,), grad_dt, param_lowp=low_dt, group=1),
+               T("frozen", (33,), grad_dt, trainable=False, param_lowp=low_dt)]
+    groups = (W.GroupSpec(lr=1e-3, weight_decay=0.01), W.GroupSpec(lr=2e-3, beta1=0.8, beta2=0.99))
+    w = _custom(tensors, groups, steps=4, grad_std=0.5)
+    run_parity(w)
+    run_parity(w, shift=[(1, 1, 1, 1)] * len(tensors), tuning=dict(update_chunk=1024, norm_chunk=2048))

@@ -24,6 +24,7 @@ import numpy as np
 
 F32 = "f32"
 BF16 = "bf16"
+F16 = "f16"
 
 
 @dataclass(frozen=True)
@@ -35,6 +36,7 @@ class TensorSpec:
     trainable: bool = True
     owned: bool = True
     zero_grad: bool = False  # every gradient element of this tensor is 0
+    param_lowp: Optional[str] = None  # BF16 / F16: a model copy of the fp32 master weights
 
     @property
     def numel(self) -> int:
@@ -82,11 +84,12 @@ class Workload:
 
     def effective_bytes_per_step(self) -> int:
         """Bytes per step under the stated accounting: 32 B per trainable
-        element with fp32 gradients, 28 B with bf16 gradients."""
+        element with fp32 gradients, 28 B with 16-bit gradients (plus 2 B for
+        a 16-bit model copy)."""
         total = 0
         for t in self.tensors:
             if t.trainable:
-                total += t.numel * (32 if t.grad_dtype == F32 else 28)
+                total += t.numel * ((32 if t.grad_dtype == F32 else 28) + (2 if t.param_lowp else 0))
         return total
 
     def algorithmic_bytes_per_step(self) -> int:
@@ -97,7 +100,7 @@ class Workload:
             if not t.trainable:
                 continue
             gb = 4 if t.grad_dtype == F32 else 2
-            total += t.numel * (gb + 24)
+            total += t.numel * (gb + 24 + (2 if t.param_lowp else 0))
             if t.owned:
                 total += t.numel * gb
         return total
@@ -144,11 +147,15 @@ def _transformer_blocks(n_blocks: int, width: int, mlp: int, grad_dtype: str,
 
 
 def action_expert(n_blocks: int = 18, width: int = 1024, mlp: int = 4096,
-                  steps: int = 10) -> Workload:
-    """~300M-parameter action-expert-like head, bf16 grads, two groups."""
+                  steps: int = 10, master: bool = False) -> Workload:
+    """~300M-parameter action-expert-like head, bf16 grads, two groups.  With
+    master=True the fp32 weights are master copies of bf16 model weights."""
+    tensors = _transformer_blocks(n_blocks, width, mlp, BF16)
+    if master:
+        tensors = tuple(replace(t, param_lowp=BF16) for t in tensors)
     return Workload(
-        name=f"action-expert-{n_blocks}x{width}x{mlp}",
-        tensors=_transformer_blocks(n_blocks, width, mlp, BF16),
+        name=f"action-expert-{n_blocks}x{width}x{mlp}" + ("-master" if master else ""),
+        tensors=tensors,
         groups=(GroupSpec(lr=5e-6, weight_decay=0.01), GroupSpec(lr=5e-6, weight_decay=0.0)),
         grad_divisor=64.0, max_norm=1.0, steps=steps, grad_std=1e-3, seed=1236)
 

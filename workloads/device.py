@@ -39,14 +39,24 @@ class FlatBuffers:
             self.G.view(torch.int16).fill_(SENTINEL_BF16)
         else:
             self.G.view(torch.int32).fill_(SENTINEL_F32)
-        self.p, self.g, self.m, self.v = [], [], [], []
+        lows = {t.param_lowp for t in w.tensors if t.param_lowp}
+        if len(lows) > 1:
+            raise ValueError("one model-copy dtype per flat workload")
+        self.PL = None
+        if lows:
+            self.PL = torch.empty(total, dtype=torch_dtype(lows.pop()), device=self.device)
+            self.PL.view(torch.int16).fill_(SENTINEL_BF16)
+        self.p, self.g, self.m, self.v, self.plow = [], [], [], [], []
         for k, t in enumerate(w.tensors):
             sl = slice(self.offsets[k], self.offsets[k] + t.numel)
             self.p.append(self.P[sl])
             self.g.append(self.G[sl])
             self.m.append(self.M[sl])
             self.v.append(self.V[sl])
+            self.plow.append(self.PL[sl] if (self.PL is not None and t.param_lowp) else None)
             self.p[-1].copy_(draw_param(w, k, self.device).reshape(-1))
+            if self.plow[-1] is not None:
+                self.plow[-1].copy_(self.p[-1].to(self.PL.dtype))
             self.m[-1].zero_()
             self.v[-1].zero_()
         self.load_grads(grad_step)
@@ -72,5 +82,7 @@ class FlatBuffers:
                 if not bool((buf.view(torch.int32)[a:b] == SENTINEL_F32).all()):
                     return False
             if not bool((gi[a:b] == gsent).all()):
+                return False
+            if self.PL is not None and not bool((self.PL.view(torch.int16)[a:b] == SENTINEL_BF16).all()):
                 return False
         return True

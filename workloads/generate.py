@@ -12,9 +12,9 @@ import hashlib
 
 import torch
 
-from .configs import BF16, F32, Workload
+from .configs import BF16, F16, F32, Workload
 
-_DTYPES = {F32: torch.float32, BF16: torch.bfloat16}
+_DTYPES = {F32: torch.float32, BF16: torch.bfloat16, F16: torch.float16}
 
 
 def torch_dtype(tag: str) -> torch.dtype:
