@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--tuning", default="", help="update_chunk,norm_chunk,ctas_per_sm")
+    ap.add_argument("--tuning", default="",
+                    help="update_chunk,norm_chunk,update_ctas_per_sm,norm_ctas_per_sm (0 = default)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step (soma_opt_step_graph) in a CUDA graph and time its replays")
     ap.add_argument("--master", action="store_true",
@@ -284,8 +285,7 @@ def run_ours(args):
     for q in w.groups:
         opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
     if args.tuning:
-        uc, nc, cps = (int(x) for x in args.tuning.split(","))
-        opt.set_tuning(uc, nc, cps)
+        opt.set_tuning(*(int(x) for x in args.tuning.split(",")))
     tl = TensorList(p, g, m, v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
                     owned=[t.owned for t in w.tensors], params_lowp=fb.plow)
     stream = torch.cuda.current_stream(device)

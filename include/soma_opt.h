@@ -239,11 +239,12 @@ soma_status_t soma_opt_get_plan(soma_opt_t opt, soma_plan_t *plan);
 
 /* Tuning knobs for benchmarks: elements per update chunk and per norm chunk
  * (rounded to a multiple of 64; 0 = automatic: 16 Ki / 64 Ki elements, less
- * for lists too small to give every SM four chunks, never below 1 Ki) and
- * resident CTAs per SM for a persistent grid (0 = one CTA per chunk).  Takes
+ * for lists too small to give every SM four chunks, never below 1 Ki) and,
+ * per kernel, resident CTAs per SM for a persistent grid (0 = one CTA per
+ * chunk).  Results do not depend on the grid, only on the chunk sizes.  Takes
  * effect at the next list (re)build. */
 soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t norm_chunk,
-                                  int32_t ctas_per_sm);
+                                  int32_t update_ctas_per_sm, int32_t norm_ctas_per_sm);
 
 /* Text of a status code (static storage). */
 const char *soma_status_string(soma_status_t status);

@@ -239,8 +239,10 @@ class SomaOpt:
         self._check(_abi.soma_opt_get_plan(self._h, ctypes.byref(p)))
         return {name: getattr(p, name) for name, _ in soma_plan_t._fields_ if name != "reserved"}
 
-    def set_tuning(self, update_chunk: int = 0, norm_chunk: int = 0, ctas_per_sm: int = 0):
-        self._check(_abi.soma_opt_set_tuning(self._h, update_chunk, norm_chunk, ctas_per_sm))
+    def set_tuning(self, update_chunk: int = 0, norm_chunk: int = 0, update_ctas_per_sm: int = 0,
+                   norm_ctas_per_sm: int = 0):
+        self._check(_abi.soma_opt_set_tuning(self._h, update_chunk, norm_chunk, update_ctas_per_sm,
+                                             norm_ctas_per_sm))
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

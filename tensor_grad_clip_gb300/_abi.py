@@ -97,7 +97,7 @@ SIGNATURES = {
     "soma_opt_set_timing": (soma_status_t, [soma_opt_t, _I32]),
     "soma_opt_read_timing": (soma_status_t, [soma_opt_t, _DP, _DP, _I64P]),
     "soma_opt_get_plan": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_plan_t)]),
-    "soma_opt_set_tuning": (soma_status_t, [soma_opt_t, _I32, _I32, _I32]),
+    "soma_opt_set_tuning": (soma_status_t, [soma_opt_t, _I32, _I32, _I32, _I32]),
     "soma_status_string": (ctypes.c_char_p, [soma_status_t]),
     "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),
     "soma_abi_version": (_I32, []),

@@ -132,54 +132,92 @@ __device__ __forceinline__ void sq4_f32(const float4 u, float& a0, float& a1) {
     a0 = fmaf(u.z, u.z, a0); a1 = fmaf(u.w, u.w, a1);
 }
 
-template <int DT>
-__device__ __forceinline__ void sumsq_16(const Seg& s, float& a0, float& a1) {
-    const uint16_t* g = static_cast<const uint16_t*>(s.g);
-    for (int j = threadIdx.x; j < s.head; j += blockDim.x) {
-        float x = one16<DT>(__ldg(g + j));
-        a0 = fmaf(x, x, a0);
+// Exclusive prefix sums over the staged segments of a chunk (at most 64):
+// upre[k] = 16-byte units of vector body in segments before k (one unit per
+// 8-element vector of a 16-bit gradient, two for fp32), spre[k] = elements
+// handled one at a time (head + tail) before k; upre[64] / spre[64] hold the
+// totals.  One warp scans, two segments per lane.
+__device__ __forceinline__ int body_units(const Seg& s) { return s.gdtype == kF32 ? 2 * s.nvec : s.nvec; }
+
+__device__ __forceinline__ void segment_prefix(const Seg* segs, int ns, int* upre, int* spre) {
+    static_assert(kMaxSegsPerChunk == 64, "two segments per lane");
+    if (threadIdx.x < 32) {
+        const unsigned full = 0xffffffffu;
+        const int l = threadIdx.x;
+        const int v0 = l < ns ? body_units(segs[l]) : 0;
+        const int v1 = l + 32 < ns ? body_units(segs[l + 32]) : 0;
+        const int s0 = l < ns ? segs[l].len - kVec * segs[l].nvec : 0;
+        const int s1 = l + 32 < ns ? segs[l + 32].len - kVec * segs[l + 32].nvec : 0;
+        int iv0 = v0, iv1 = v1, is0 = s0, is1 = s1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t;
+            t = __shfl_up_sync(full, iv0, o); if (l >= o) iv0 += t;
+            t = __shfl_up_sync(full, iv1, o); if (l >= o) iv1 += t;
+            t = __shfl_up_sync(full, is0, o); if (l >= o) is0 += t;
+            t = __shfl_up_sync(full, is1, o); if (l >= o) is1 += t;
+        }
+        const int tv0 = __shfl_sync(full, iv0, 31), ts0 = __shfl_sync(full, is0, 31);
+        upre[l] = iv0 - v0;
+        upre[l + 32] = tv0 + iv1 - v1;
+        spre[l] = is0 - s0;
+        spre[l + 32] = ts0 + is1 - s1;
+        if (l == 31) {
+            upre[64] = tv0 + iv1;
+            spre[64] = ts0 + is1;
+        }
     }
-    const uint4* gv = reinterpret_cast<const uint4*>(g + s.head);
-    const int S = blockDim.x;
-    int i = threadIdx.x;
-    for (; i + 3 * S < s.nvec; i += 4 * S) {  // four independent 16-byte loads in flight
-        const uint4 w0 = __ldg(gv + i), w1 = __ldg(gv + i + S);
-        const uint4 w2 = __ldg(gv + i + 2 * S), w3 = __ldg(gv + i + 3 * S);
-        sq8_16<DT>(w0, a0, a1);
-        sq8_16<DT>(w1, a0, a1);
-        sq8_16<DT>(w2, a0, a1);
-        sq8_16<DT>(w3, a0, a1);
-    }
-    for (; i < s.nvec; i += S) sq8_16<DT>(__ldg(gv + i), a0, a1);
-    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
-        float x = one16<DT>(__ldg(g + j));
-        a1 = fmaf(x, x, a1);
-    }
+    __syncthreads();
 }
 
-__device__ __forceinline__ void sumsq_f32(const Seg& s, float& a0, float& a1) {
-    const float* g = static_cast<const float*>(s.g);
-    for (int j = threadIdx.x; j < s.head; j += blockDim.x) {
-        float x = __ldg(g + j);
-        a0 = fmaf(x, x, a0);
+// Square-sum of one chunk.  The 16-byte units of all its segments' vector
+// bodies form one index space; thread t takes units t, t + B, t + 2B, ...
+// (B = block size), four loads in flight whatever the segment sizes, and
+// follows its segment with a cursor that only moves forward.  The head and
+// tail elements are flattened the same way.
+__device__ __forceinline__ void chunk_sumsq(const Seg* segs, const int* upre, const int* spre, float& a0,
+                                            float& a1) {
+    const int B = blockDim.x;
+    const int U = upre[kMaxSegsPerChunk];
+    int k = 0;
+    for (int u0 = threadIdx.x; u0 < U; u0 += 4 * B) {
+        uint4 w[4];
+        uint8_t dt[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int u = u0 + q * B;
+            dt[q] = 0xff;
+            if (u < U) {
+                while (u >= upre[k + 1]) ++k;
+                const Seg& sg = segs[k];
+                dt[q] = sg.gdtype;
+                const char* base = static_cast<const char*>(sg.g) + sg.head * (sg.gdtype == kF32 ? 4 : 2);
+                w[q] = __ldg(reinterpret_cast<const uint4*>(base) + (u - upre[k]));
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (dt[q] == kF32) {
+                sq4_f32(make_float4(__uint_as_float(w[q].x), __uint_as_float(w[q].y), __uint_as_float(w[q].z),
+                                    __uint_as_float(w[q].w)), a0, a1);
+            } else if (dt[q] == kBF16) {
+                sq8_16<kBF16>(w[q], a0, a1);
+            } else if (dt[q] == kF16) {
+                sq8_16<kF16>(w[q], a0, a1);
+            }
+        }
     }
-    const float4* gv = reinterpret_cast<const float4*>(g + s.head);
-    const int S = blockDim.x;
-    int i = threadIdx.x;
-    for (; i + S < s.nvec; i += 2 * S) {  // four independent 16-byte loads in flight
-        const float4 u0 = __ldg(gv + 2 * i), w0 = __ldg(gv + 2 * i + 1);
-        const float4 u1 = __ldg(gv + 2 * (i + S)), w1 = __ldg(gv + 2 * (i + S) + 1);
-        sq4_f32(u0, a0, a1);
-        sq4_f32(w0, a0, a1);
-        sq4_f32(u1, a0, a1);
-        sq4_f32(w1, a0, a1);
-    }
-    if (i < s.nvec) {
-        sq4_f32(__ldg(gv + 2 * i), a0, a1);
-        sq4_f32(__ldg(gv + 2 * i + 1), a0, a1);
-    }
-    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x) {
-        float x = __ldg(g + j);
+    const int S = spre[kMaxSegsPerChunk];
+    k = 0;
+    for (int e = threadIdx.x; e < S; e += B) {
+        while (e >= spre[k + 1]) ++k;
+        const Seg& sg = segs[k];
+        const int j = e - spre[k];
+        const int idx = j < sg.head ? j : sg.head + kVec * sg.nvec + (j - sg.head);
+        float x;
+        if (sg.gdtype == kF32) x = __ldg(static_cast<const float*>(sg.g) + idx);
+        else if (sg.gdtype == kBF16) x = bf16_one(__ldg(static_cast<const uint16_t*>(sg.g) + idx));
+        else x = f16_one(__ldg(static_cast<const uint16_t*>(sg.g) + idx));
         a1 = fmaf(x, x, a1);
     }
 }
@@ -202,20 +240,18 @@ __device__ __forceinline__ GroupHp group_constants(const DevGroup& g, int64_t t)
 }
 
 template <bool kGraph>
-__global__ void __launch_bounds__(kNormBlock) norm_kernel(const __grid_constant__ NormArgs a) {
+__global__ void __launch_bounds__(kNormBlock, 4) norm_kernel(const __grid_constant__ NormArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
+    __shared__ int upre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
     __shared__ float wsum[kNormBlock / 32];
     __shared__ double wsum64[kNormBlock / 32];
     __shared__ int last;
 
     for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
         const int ns = stage_segments(a.t, c, segs);
+        segment_prefix(segs, ns, upre, spre);
         float a0 = 0.f, a1 = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            if (segs[s].gdtype == kBF16) sumsq_16<kBF16>(segs[s], a0, a1);
-            else if (segs[s].gdtype == kF16) sumsq_16<kF16>(segs[s], a0, a1);
-            else sumsq_f32(segs[s], a0, a1);
-        }
+        chunk_sumsq(segs, upre, spre, a0, a1);
         const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
         if (threadIdx.x == 0) a.partials[c] = (double)bs;
         __syncthreads();  // segs and wsum are reused by the next chunk

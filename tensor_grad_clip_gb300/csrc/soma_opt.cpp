@@ -56,7 +56,8 @@ struct soma_opt {
 
     int32_t update_chunk = 0;       // 0: automatic (see chunk_size)
     int32_t norm_chunk = 0;
-    int32_t ctas_per_sm = 0;
+    int32_t update_ctas_per_sm = 0; // 0: one CTA per chunk
+    int32_t norm_ctas_per_sm = 0;
 
     // device state, created on first use
     bool dev_ready = false;
@@ -347,9 +348,10 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
                              reinterpret_cast<const int32_t*>(d + o_ub), upd.nchunks()};
     o->norm_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_ns),
                               reinterpret_cast<const int32_t*>(d + o_nb), nrm.nchunks()};
-    const int64_t cap = o->ctas_per_sm > 0 ? (int64_t)o->sm_count * o->ctas_per_sm : INT32_MAX;
-    o->upd_grid = (int)std::min<int64_t>(upd.nchunks(), cap);
-    o->norm_grid = (int)std::max<int64_t>(1, std::min<int64_t>(nrm.nchunks(), cap));
+    const int64_t ucap = o->update_ctas_per_sm > 0 ? (int64_t)o->sm_count * o->update_ctas_per_sm : INT32_MAX;
+    const int64_t ncap = o->norm_ctas_per_sm > 0 ? (int64_t)o->sm_count * o->norm_ctas_per_sm : INT32_MAX;
+    o->upd_grid = (int)std::min<int64_t>(upd.nchunks(), ucap);
+    o->norm_grid = (int)std::max<int64_t>(1, std::min<int64_t>(nrm.nchunks(), ncap));
     o->group_present = present;
     o->cached.assign(list, list + n);
     o->cache_valid = true;
@@ -539,17 +541,20 @@ soma_status_t soma_opt_set_group_step(soma_opt_t h, int32_t group, int64_t t) {
     return SOMA_OK;
 }
 
-soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t norm_chunk, int32_t ctas_per_sm) {
+soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t norm_chunk,
+                                  int32_t update_ctas_per_sm, int32_t norm_ctas_per_sm) {
     soma_opt* o = live_handle(h);
     if (!o) return SOMA_ERR_STATE;
     auto ok_chunk = [](int32_t c) { return c == 0 || (c >= 64 && c <= (1 << 26)); };
     if (!ok_chunk(update_chunk) || !ok_chunk(norm_chunk))
         return o->fail(SOMA_ERR_INVALID_ARG, "chunk sizes must be 0 or in [64, 2^26]");
-    if (ctas_per_sm < 0 || ctas_per_sm > 64) return o->fail(SOMA_ERR_INVALID_ARG, "ctas_per_sm must be in [0, 64]");
+    if (update_ctas_per_sm < 0 || update_ctas_per_sm > 64 || norm_ctas_per_sm < 0 || norm_ctas_per_sm > 64)
+        return o->fail(SOMA_ERR_INVALID_ARG, "CTAs per SM must be in [0, 64]");
     if (o->graph_locked) return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: its plan is fixed");
     o->update_chunk = update_chunk / 64 * 64;
     o->norm_chunk = norm_chunk / 64 * 64;
-    o->ctas_per_sm = ctas_per_sm;
+    o->update_ctas_per_sm = update_ctas_per_sm;
+    o->norm_ctas_per_sm = norm_ctas_per_sm;
     o->cache_valid = false;
     return SOMA_OK;
 }

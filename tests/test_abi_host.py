@@ -193,8 +193,9 @@ def test_use_after_destroy_and_null_handle():
 
 def test_tuning_and_timing_arguments():
     opt = SomaOpt(0)
-    opt.set_tuning(update_chunk=4096, norm_chunk=8192, ctas_per_sm=4)
-    for bad in (dict(update_chunk=10), dict(norm_chunk=1 << 27), dict(ctas_per_sm=-1), dict(ctas_per_sm=65)):
+    opt.set_tuning(update_chunk=4096, norm_chunk=8192, update_ctas_per_sm=2, norm_ctas_per_sm=4)
+    for bad in (dict(update_chunk=10), dict(norm_chunk=1 << 27), dict(update_ctas_per_sm=-1),
+                dict(norm_ctas_per_sm=65)):
         with pytest.raises(SomaError):
             opt.set_tuning(**bad)
     assert _abi.soma_opt_set_timing(opt.handle, 2) == _abi.SOMA_ERR_INVALID_ARG

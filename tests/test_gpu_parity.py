@@ -35,9 +35,9 @@ def test_many_chunks_and_persistent_grid():
     # Tiny chunks force hundreds of chunks and segments that straddle tensors;
     # a persistent grid (fewer CTAs than chunks) must give the same bits.
     w = W.with_steps(W.SMALL["action_expert"](), 3)
-    run_parity(w, tuning=dict(update_chunk=640, norm_chunk=1024, ctas_per_sm=0))
-    a = _final_state(w, dict(update_chunk=2048, norm_chunk=4096, ctas_per_sm=0))
-    b = _final_state(w, dict(update_chunk=2048, norm_chunk=4096, ctas_per_sm=1))
+    run_parity(w, tuning=dict(update_chunk=640, norm_chunk=1024))
+    a = _final_state(w, dict(update_chunk=2048, norm_chunk=4096))
+    b = _final_state(w, dict(update_chunk=2048, norm_chunk=4096, update_ctas_per_sm=1, norm_ctas_per_sm=1))
     for x, y in zip(a, b):
         assert torch.equal(x, y)
 
