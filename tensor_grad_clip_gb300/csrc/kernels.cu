@@ -137,15 +137,21 @@ __device__ __forceinline__ void sq4_f32(const float4 u, float& a0, float& a1) {
 // 8-element vector of a 16-bit gradient, two for fp32), spre[k] = elements
 // handled one at a time (head + tail) before k; upre[64] / spre[64] hold the
 // totals.  One warp scans, two segments per lane.
-__device__ __forceinline__ int body_units(const Seg& s) { return s.gdtype == kF32 ? 2 * s.nvec : s.nvec; }
+// kUnits: count 16-byte units of gradient (square-sum); otherwise count
+// 8-element vectors (update).
+template <bool kUnits>
+__device__ __forceinline__ int body_count(const Seg& s) {
+    return (kUnits && s.gdtype == kF32) ? 2 * s.nvec : s.nvec;
+}
 
+template <bool kUnits>
 __device__ __forceinline__ void segment_prefix(const Seg* segs, int ns, int* upre, int* spre) {
     static_assert(kMaxSegsPerChunk == 64, "two segments per lane");
     if (threadIdx.x < 32) {
         const unsigned full = 0xffffffffu;
         const int l = threadIdx.x;
-        const int v0 = l < ns ? body_units(segs[l]) : 0;
-        const int v1 = l + 32 < ns ? body_units(segs[l + 32]) : 0;
+        const int v0 = l < ns ? body_count<kUnits>(segs[l]) : 0;
+        const int v1 = l + 32 < ns ? body_count<kUnits>(segs[l + 32]) : 0;
         const int s0 = l < ns ? segs[l].len - kVec * segs[l].nvec : 0;
         const int s1 = l + 32 < ns ? segs[l + 32].len - kVec * segs[l + 32].nvec : 0;
         int iv0 = v0, iv1 = v1, is0 = s0, is1 = s1;
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kNormBlock, 4) norm_kernel(const __grid_consta
 
     for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
         const int ns = stage_segments(a.t, c, segs);
-        segment_prefix(segs, ns, upre, spre);
+        segment_prefix<true>(segs, ns, upre, spre);
         float a0 = 0.f, a1 = 0.f;
         chunk_sumsq(segs, upre, spre, a0, a1);
         const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
@@ -329,110 +335,191 @@ __device__ __forceinline__ void adamw(float& p, float& m, float& v, float g, con
     p = fmaf(-h.step_size, m / denom, p);
 }
 
-template <int DT>
-__device__ __forceinline__ float grad_one(const Seg& s, int j) {
-    if (DT == kF32) return __ldcs(static_cast<const float*>(s.g) + j);
-    return one16<DT>(__ldcs(static_cast<const unsigned short*>(s.g) + j));
-}
-
-template <int DT, int LOW>
+// One element j of a segment, any gradient and copy dtype.
 __device__ __forceinline__ void update_one(const Seg& s, int j, const GroupHp& h, float scale) {
+    float g;
+    if (s.gdtype == kF32) g = __ldcs(static_cast<const float*>(s.g) + j);
+    else if (s.gdtype == kBF16) g = bf16_one(__ldcs(static_cast<const unsigned short*>(s.g) + j));
+    else g = f16_one(__ldcs(static_cast<const unsigned short*>(s.g) + j));
     float p = __ldcs(s.p + j), m = __ldcs(s.m + j), v = __ldcs(s.v + j);
-    adamw(p, m, v, grad_one<DT>(s, j) * scale, h);
+    adamw(p, m, v, g * scale, h);
     __stcs(s.p + j, p);
     __stcs(s.m + j, m);
     __stcs(s.v + j, v);
-    if (LOW != kNone) __stcs(static_cast<unsigned short*>(s.plow) + j, one_to16<LOW>(p));
+    if (s.lowdt == kBF16) __stcs(static_cast<unsigned short*>(s.plow) + j, one_to16<kBF16>(p));
+    else if (s.lowdt == kF16) __stcs(static_cast<unsigned short*>(s.plow) + j, one_to16<kF16>(p));
 }
 
+// Eight consecutive elements of the vector body: raw gradient words as
+// loaded (one 16-byte word for 16-bit gradients, two for fp32) and p, m, v.
 struct Lane8 {
-    float g[8];
+    uint4 g0, g1;
     float4 p0, p1, m0, m1, v0, v1;
 };
 
 template <int DT>
-__device__ __forceinline__ void load8(const Seg& s, int i, Lane8& x) {
+__device__ __forceinline__ void load8_t(const Seg& s, int i, Lane8& x) {
     const float4* p = reinterpret_cast<const float4*>(s.p + s.head) + 2 * i;
     const float4* m = reinterpret_cast<const float4*>(s.m + s.head) + 2 * i;
     const float4* v = reinterpret_cast<const float4*>(s.v + s.head) + 2 * i;
     if (DT == kF32) {
-        const float4* g = reinterpret_cast<const float4*>(static_cast<const float*>(s.g) + s.head) + 2 * i;
-        const float4 u = __ldcs(g), w = __ldcs(g + 1);
-        x.g[0] = u.x; x.g[1] = u.y; x.g[2] = u.z; x.g[3] = u.w;
-        x.g[4] = w.x; x.g[5] = w.y; x.g[6] = w.z; x.g[7] = w.w;
+        const uint4* g = reinterpret_cast<const uint4*>(static_cast<const float*>(s.g) + s.head) + 2 * i;
+        x.g0 = __ldcs(g);
+        x.g1 = __ldcs(g + 1);
     } else {
-        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(
-                                   static_cast<const uint16_t*>(s.g) + s.head) + i);
-        float2 t;
-        t = pair16<DT>(w.x); x.g[0] = t.x; x.g[1] = t.y;
-        t = pair16<DT>(w.y); x.g[2] = t.x; x.g[3] = t.y;
-        t = pair16<DT>(w.z); x.g[4] = t.x; x.g[5] = t.y;
-        t = pair16<DT>(w.w); x.g[6] = t.x; x.g[7] = t.y;
+        x.g0 = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(s.g) + s.head) + i);
     }
     x.p0 = __ldcs(p); x.p1 = __ldcs(p + 1);
     x.m0 = __ldcs(m); x.m1 = __ldcs(m + 1);
     x.v0 = __ldcs(v); x.v1 = __ldcs(v + 1);
 }
 
-__device__ __forceinline__ void compute8(Lane8& x, const GroupHp& h, float scale) {
-    adamw(x.p0.x, x.m0.x, x.v0.x, x.g[0] * scale, h);
-    adamw(x.p0.y, x.m0.y, x.v0.y, x.g[1] * scale, h);
-    adamw(x.p0.z, x.m0.z, x.v0.z, x.g[2] * scale, h);
-    adamw(x.p0.w, x.m0.w, x.v0.w, x.g[3] * scale, h);
-    adamw(x.p1.x, x.m1.x, x.v1.x, x.g[4] * scale, h);
-    adamw(x.p1.y, x.m1.y, x.v1.y, x.g[5] * scale, h);
-    adamw(x.p1.z, x.m1.z, x.v1.z, x.g[6] * scale, h);
-    adamw(x.p1.w, x.m1.w, x.v1.w, x.g[7] * scale, h);
+__device__ __forceinline__ void load8(const Seg& s, int i, Lane8& x) {
+    if (s.gdtype == kF32) load8_t<kF32>(s, i, x);
+    else load8_t<kBF16>(s, i, x);  // one 16-byte word for either 16-bit type
+}
+
+template <int DT>
+__device__ __forceinline__ void widen8(const Lane8& x, float (&g)[8]) {
+    if (DT == kF32) {
+        g[0] = __uint_as_float(x.g0.x); g[1] = __uint_as_float(x.g0.y);
+        g[2] = __uint_as_float(x.g0.z); g[3] = __uint_as_float(x.g0.w);
+        g[4] = __uint_as_float(x.g1.x); g[5] = __uint_as_float(x.g1.y);
+        g[6] = __uint_as_float(x.g1.z); g[7] = __uint_as_float(x.g1.w);
+    } else {
+        float2 t;
+        t = pair16<DT>(x.g0.x); g[0] = t.x; g[1] = t.y;
+        t = pair16<DT>(x.g0.y); g[2] = t.x; g[3] = t.y;
+        t = pair16<DT>(x.g0.z); g[4] = t.x; g[5] = t.y;
+        t = pair16<DT>(x.g0.w); g[6] = t.x; g[7] = t.y;
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void compute8_t(Lane8& x, const GroupHp& h, float scale) {
+    float g[8];
+    widen8<DT>(x, g);
+    adamw(x.p0.x, x.m0.x, x.v0.x, g[0] * scale, h);
+    adamw(x.p0.y, x.m0.y, x.v0.y, g[1] * scale, h);
+    adamw(x.p0.z, x.m0.z, x.v0.z, g[2] * scale, h);
+    adamw(x.p0.w, x.m0.w, x.v0.w, g[3] * scale, h);
+    adamw(x.p1.x, x.m1.x, x.v1.x, g[4] * scale, h);
+    adamw(x.p1.y, x.m1.y, x.v1.y, g[5] * scale, h);
+    adamw(x.p1.z, x.m1.z, x.v1.z, g[6] * scale, h);
+    adamw(x.p1.w, x.m1.w, x.v1.w, g[7] * scale, h);
+}
+
+__device__ __forceinline__ void compute8(const Seg& s, Lane8& x, const GroupHp& h, float scale) {
+    if (s.gdtype == kF32) compute8_t<kF32>(x, h, scale);
+    else if (s.gdtype == kBF16) compute8_t<kBF16>(x, h, scale);
+    else compute8_t<kF16>(x, h, scale);
 }
 
 template <int LOW>
-__device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
+__device__ __forceinline__ uint4 pack8(const Lane8& x) {
+    uint4 w;
+    w.x = pack16<LOW>(x.p0.x, x.p0.y);
+    w.y = pack16<LOW>(x.p0.z, x.p0.w);
+    w.z = pack16<LOW>(x.p1.x, x.p1.y);
+    w.w = pack16<LOW>(x.p1.z, x.p1.w);
+    return w;
+}
+
+template <int LOW>
+__device__ __forceinline__ void store8_t(const Seg& s, int i, const Lane8& x) {
     float4* p = reinterpret_cast<float4*>(s.p + s.head) + 2 * i;
     float4* m = reinterpret_cast<float4*>(s.m + s.head) + 2 * i;
     float4* v = reinterpret_cast<float4*>(s.v + s.head) + 2 * i;
     __stcs(p, x.p0); __stcs(p + 1, x.p1);
     __stcs(m, x.m0); __stcs(m + 1, x.m1);
     __stcs(v, x.v0); __stcs(v + 1, x.v1);
-    if (LOW != kNone) {
-        uint4 w;
-        w.x = pack16<LOW>(x.p0.x, x.p0.y);
-        w.y = pack16<LOW>(x.p0.z, x.p0.w);
-        w.z = pack16<LOW>(x.p1.x, x.p1.y);
-        w.w = pack16<LOW>(x.p1.z, x.p1.w);
-        __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.plow) + s.head) + i, w);
-    }
+    if (LOW != kNone)
+        __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.plow) + s.head) + i, pack8<LOW>(x));
 }
 
+__device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
+    if (s.lowdt == kBF16) store8_t<kBF16>(s, i, x);
+    else if (s.lowdt == kF16) store8_t<kF16>(s, i, x);
+    else store8_t<kNone>(s, i, x);
+}
+
+// A chunk made of one segment (a slice of a large tensor): dtypes fixed at
+// compile time, two vectors in flight per thread.
 template <int DT, int LOW>
-__device__ __forceinline__ void update_segment(const Seg& s, const GroupHp& h, float scale) {
-    for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one<DT, LOW>(s, j, h, scale);
-    const int n = s.nvec;
-    const int stride = blockDim.x;
+__device__ __forceinline__ void segment_update(const Seg& s, const GroupHp& h, float scale) {
+    for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one(s, j, h, scale);
+    const int n = s.nvec, B = blockDim.x;
     int i = threadIdx.x;
-    for (; i + stride < n; i += 2 * stride) {  // two vectors in flight per thread
+    for (; i + B < n; i += 2 * B) {
         Lane8 x0, x1;
-        load8<DT>(s, i, x0);
-        load8<DT>(s, i + stride, x1);
-        compute8(x0, h, scale);
-        compute8(x1, h, scale);
-        store8<LOW>(s, i, x0);
-        store8<LOW>(s, i + stride, x1);
+        load8_t<DT>(s, i, x0);
+        load8_t<DT>(s, i + B, x1);
+        compute8_t<DT>(x0, h, scale);
+        compute8_t<DT>(x1, h, scale);
+        store8_t<LOW>(s, i, x0);
+        store8_t<LOW>(s, i + B, x1);
     }
     if (i < n) {
         Lane8 x0;
-        load8<DT>(s, i, x0);
-        compute8(x0, h, scale);
-        store8<LOW>(s, i, x0);
+        load8_t<DT>(s, i, x0);
+        compute8_t<DT>(x0, h, scale);
+        store8_t<LOW>(s, i, x0);
     }
-    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += blockDim.x)
-        update_one<DT, LOW>(s, j, h, scale);
+    for (int j = s.head + kVec * s.nvec + threadIdx.x; j < s.len; j += B) update_one(s, j, h, scale);
 }
 
 template <int DT>
-__device__ __forceinline__ void update_segment_low(const Seg& s, const GroupHp& h, float scale) {
-    if (s.lowdt == kBF16) update_segment<DT, kBF16>(s, h, scale);
-    else if (s.lowdt == kF16) update_segment<DT, kF16>(s, h, scale);
-    else update_segment<DT, kNone>(s, h, scale);
+__device__ __forceinline__ void segment_update_low(const Seg& s, const GroupHp& h, float scale) {
+    if (s.lowdt == kBF16) segment_update<DT, kBF16>(s, h, scale);
+    else if (s.lowdt == kF16) segment_update<DT, kF16>(s, h, scale);
+    else segment_update<DT, kNone>(s, h, scale);
+}
+
+// One chunk of the update.  The 8-element vectors of all its segments form
+// one index space; thread t takes vectors t, t + B, t + 2B, ... two at a
+// time (both loaded before either is used), following its segment with a
+// forward-only cursor, so small tensors keep as many loads in flight as
+// large ones.  Head and tail elements are flattened the same way.
+template <bool kGraph>
+__device__ __forceinline__ void chunk_update(const Seg* segs, const int* vpre, const int* spre,
+                                             const UpdateArgs& a, const GroupHp* shp, float scale) {
+    const int B = blockDim.x;
+    const int V = vpre[kMaxSegsPerChunk];
+    int k = 0;
+    for (int v0 = threadIdx.x; v0 < V; v0 += 2 * B) {
+        Lane8 x0, x1;
+        const int v1 = v0 + B;
+        while (v0 >= vpre[k + 1]) ++k;
+        const int k0 = k;
+        load8(segs[k0], v0 - vpre[k0], x0);
+        int k1 = -1;
+        if (v1 < V) {
+            while (v1 >= vpre[k + 1]) ++k;
+            k1 = k;
+            load8(segs[k1], v1 - vpre[k1], x1);
+        }
+        {
+            const Seg& s = segs[k0];
+            const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
+            compute8(s, x0, h, scale);
+            store8(s, v0 - vpre[k0], x0);
+        }
+        if (k1 >= 0) {
+            const Seg& s = segs[k1];
+            const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
+            compute8(s, x1, h, scale);
+            store8(s, v1 - vpre[k1], x1);
+        }
+    }
+    const int S = spre[kMaxSegsPerChunk];
+    k = 0;
+    for (int e = threadIdx.x; e < S; e += B) {
+        while (e >= spre[k + 1]) ++k;
+        const Seg& s = segs[k];
+        const int j = e - spre[k];
+        const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
+        update_one(s, j < s.head ? j : s.head + kVec * s.nvec + (j - s.head), h, scale);
+    }
 }
 
 // Chunks run in reverse list order: the gradients the square-sum kernel read
@@ -440,6 +527,7 @@ __device__ __forceinline__ void update_segment_low(const Seg& s, const GroupHp& 
 template <bool kGraph>
 __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_constant__ UpdateArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
+    __shared__ int vpre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
     __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
     const float scale = __ldcg(&a.res->scale);
     if (kGraph) {  // made visible by the first __syncthreads in stage_segments
@@ -448,14 +536,17 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
     for (int r = blockIdx.x; r < a.t.nchunks; r += gridDim.x) {
         const int c = a.t.nchunks - 1 - r;
         const int ns = stage_segments(a.t, c, segs);
-        for (int k = 0; k < ns; ++k) {
-            const Seg& s = segs[k];
+        if (ns == 1) {
+            const Seg& s = segs[0];
             const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
-            if (s.gdtype == kBF16) update_segment_low<kBF16>(s, h, scale);
-            else if (s.gdtype == kF16) update_segment_low<kF16>(s, h, scale);
-            else update_segment_low<kF32>(s, h, scale);
+            if (s.gdtype == kBF16) segment_update_low<kBF16>(s, h, scale);
+            else if (s.gdtype == kF16) segment_update_low<kF16>(s, h, scale);
+            else segment_update_low<kF32>(s, h, scale);
+        } else {
+            segment_prefix<false>(segs, ns, vpre, spre);
+            chunk_update<kGraph>(segs, vpre, spre, a, shp, scale);
         }
-        __syncthreads();  // segs is restaged for the next chunk
+        __syncthreads();  // segs and the prefixes are rebuilt for the next chunk
     }
 }
 
