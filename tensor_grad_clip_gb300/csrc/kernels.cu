@@ -253,6 +253,10 @@ __global__ void __launch_bounds__(kNormBlock, 4) norm_kernel(const __grid_consta
     __shared__ double wsum64[kNormBlock / 32];
     __shared__ int last;
 
+    // The update kernel may be scheduled as soon as every CTA of this one
+    // has started; it waits for this grid's results before using them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
         const int ns = stage_segments(a.t, c, segs);
         segment_prefix<true>(segs, ns, upre, spre);
@@ -443,6 +447,18 @@ __device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
     else store8_t<kNone>(s, i, x);
 }
 
+// L2 prefetch of the gradient, p, m and v of this thread's first two vectors.
+__device__ __forceinline__ void prefetch_vectors(const Seg& s) {
+    const int gsz = s.gdtype == kF32 ? 4 : 2;
+    for (int i = threadIdx.x, n = 0; i < s.nvec && n < 2; i += blockDim.x, ++n) {
+        const int e = s.head + kVec * i;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(s.g) + (size_t)e * gsz));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(s.p + e));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(s.m + e));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(s.v + e));
+    }
+}
+
 // A chunk made of one segment (a slice of a large tensor): dtypes fixed at
 // compile time, two vectors in flight per thread.
 template <int DT, int LOW>
@@ -529,13 +545,26 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     __shared__ int vpre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
     __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
-    const float scale = __ldcg(&a.res->scale);
-    if (kGraph) {  // made visible by the first __syncthreads in stage_segments
-        for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x) shp[q] = a.dhp[q];
-    }
+    float scale = 0.f;
+    bool ready = false;
     for (int r = blockIdx.x; r < a.t.nchunks; r += gridDim.x) {
         const int c = a.t.nchunks - 1 - r;
         const int ns = stage_segments(a.t, c, segs);
+        if (!ready) {
+            // Up to here only the tables and the caller's buffers were read, so
+            // this can overlap the tail of the square-sum kernel (launched with
+            // programmatic stream serialization).  Warm L2 with this thread's
+            // first two vectors, then wait for that kernel's results: the clip
+            // scale and, for graph steps, the group constants.
+            if (ns == 1) prefetch_vectors(segs[0]);
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            scale = __ldcg(&a.res->scale);
+            if (kGraph) {
+                for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x) shp[q] = a.dhp[q];
+                __syncthreads();
+            }
+            ready = true;
+        }
         if (ns == 1) {
             const Seg& s = segs[0];
             const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
@@ -558,9 +587,20 @@ int launch_norm(const NormArgs& a, int grid, void* stream, bool graph) {
     return (int)cudaGetLastError();
 }
 
-int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph) {
-    if (graph) update_kernel<true><<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    else update_kernel<false><<<grid, kUpdateBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph, bool overlap) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kUpdateBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    cudaError_t e = graph ? cudaLaunchKernelEx(&cfg, update_kernel<true>, a)
+                          : cudaLaunchKernelEx(&cfg, update_kernel<false>, a);
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 

@@ -127,7 +127,10 @@ constexpr int kUpdateBlock = 256;
 // graph = true selects the variants that take group constants from device
 // memory (NormArgs::dgroups / dhp, UpdateArgs::dhp).
 int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false);
-int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false);
+// overlap = true launches with programmatic stream serialization: the update
+// kernel may start while the previous kernel on the stream finishes, and waits
+// (griddepcontrol.wait) before it reads that kernel's results.
+int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false, bool overlap = false);
 int launch_finish(const FinishArgs& a, void* stream);
 
 }  // namespace soma

@@ -643,7 +643,10 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
     }
     if (ev && (e = cudaEventRecord((*ev)[1], (cudaStream_t)stream)) != cudaSuccess)
         return o->cuda_fail(e, "cudaEventRecord");
-    if (o->upd_grid > 0 && (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream)) != cudaSuccess)
+    // without a timing event between the two kernels, the update kernel may
+    // overlap the square-sum kernel's tail
+    if (o->upd_grid > 0 &&
+        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, false, ev == nullptr)) != cudaSuccess)
         return o->cuda_fail(e, "launching the update kernel");
     if (ev) {
         if ((e = cudaEventRecord((*ev)[2], (cudaStream_t)stream)) != cudaSuccess)
