@@ -176,6 +176,51 @@ __device__ __forceinline__ void segment_prefix(const Seg* segs, int ns, int* upr
     __syncthreads();
 }
 
+// Square-sum of a chunk made of one segment: the gradient dtype is fixed at
+// compile time and each thread walks units t, t + B, ... four at a time.
+template <int DT>
+__device__ __forceinline__ void segment_sumsq(const Seg& s, float& a0, float& a1) {
+    const int B = blockDim.x;
+    const int esize = DT == kF32 ? 4 : 2;
+    const uint4* base = reinterpret_cast<const uint4*>(static_cast<const char*>(s.g) + s.head * esize);
+    const int U = DT == kF32 ? 2 * s.nvec : s.nvec;
+    int u = threadIdx.x;
+    for (; u + 3 * B < U; u += 4 * B) {
+        const uint4 w0 = __ldg(base + u), w1 = __ldg(base + u + B);
+        const uint4 w2 = __ldg(base + u + 2 * B), w3 = __ldg(base + u + 3 * B);
+        if (DT == kF32) {
+            sq4_f32(make_float4(__uint_as_float(w0.x), __uint_as_float(w0.y), __uint_as_float(w0.z),
+                                __uint_as_float(w0.w)), a0, a1);
+            sq4_f32(make_float4(__uint_as_float(w1.x), __uint_as_float(w1.y), __uint_as_float(w1.z),
+                                __uint_as_float(w1.w)), a0, a1);
+            sq4_f32(make_float4(__uint_as_float(w2.x), __uint_as_float(w2.y), __uint_as_float(w2.z),
+                                __uint_as_float(w2.w)), a0, a1);
+            sq4_f32(make_float4(__uint_as_float(w3.x), __uint_as_float(w3.y), __uint_as_float(w3.z),
+                                __uint_as_float(w3.w)), a0, a1);
+        } else {
+            sq8_16<DT>(w0, a0, a1);
+            sq8_16<DT>(w1, a0, a1);
+            sq8_16<DT>(w2, a0, a1);
+            sq8_16<DT>(w3, a0, a1);
+        }
+    }
+    for (; u < U; u += B) {
+        const uint4 w = __ldg(base + u);
+        if (DT == kF32)
+            sq4_f32(make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                __uint_as_float(w.w)), a0, a1);
+        else
+            sq8_16<DT>(w, a0, a1);
+    }
+    for (int j = threadIdx.x; j < s.len - kVec * s.nvec; j += B) {  // head, then tail
+        const int idx = j < s.head ? j : s.head + kVec * s.nvec + (j - s.head);
+        float x;
+        if (DT == kF32) x = __ldg(static_cast<const float*>(s.g) + idx);
+        else x = one16<DT>(__ldg(static_cast<const uint16_t*>(s.g) + idx));
+        a1 = fmaf(x, x, a1);
+    }
+}
+
 // Square-sum of one chunk.  The 16-byte units of all its segments' vector
 // bodies form one index space; thread t takes units t, t + B, t + 2B, ...
 // (B = block size), four loads in flight whatever the segment sizes, and
@@ -246,7 +291,7 @@ __device__ __forceinline__ GroupHp group_constants(const DevGroup& g, int64_t t)
 }
 
 template <bool kGraph>
-__global__ void __launch_bounds__(kNormBlock, 4) norm_kernel(const __grid_constant__ NormArgs a) {
+__global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_constant__ NormArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     __shared__ int upre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
     __shared__ float wsum[kNormBlock / 32];
@@ -259,9 +304,15 @@ __global__ void __launch_bounds__(kNormBlock, 4) norm_kernel(const __grid_consta
 
     for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
         const int ns = stage_segments(a.t, c, segs);
-        segment_prefix<true>(segs, ns, upre, spre);
         float a0 = 0.f, a1 = 0.f;
-        chunk_sumsq(segs, upre, spre, a0, a1);
+        if (ns == 1) {
+            if (segs[0].gdtype == kBF16) segment_sumsq<kBF16>(segs[0], a0, a1);
+            else if (segs[0].gdtype == kF16) segment_sumsq<kF16>(segs[0], a0, a1);
+            else segment_sumsq<kF32>(segs[0], a0, a1);
+        } else {
+            segment_prefix<true>(segs, ns, upre, spre);
+            chunk_sumsq(segs, upre, spre, a0, a1);
+        }
         const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
         if (threadIdx.x == 0) a.partials[c] = (double)bs;
         __syncthreads();  // segs and wsum are reused by the next chunk
