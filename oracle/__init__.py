@@ -46,6 +46,7 @@ class _Group(ctypes.Structure):
         ("eps", ctypes.c_double),
         ("weight_decay", ctypes.c_double),
         ("step", ctypes.c_int64),
+        ("divisor", ctypes.c_double),
     ]
 
 
@@ -140,6 +141,7 @@ class GroupState:
     eps: float = 1e-8
     weight_decay: float = 0.0
     step: int = 0
+    divisor: float = 0.0  # the group's own effective-batch divisor; 0 = the step's
 
 
 class OracleOptimizer:
@@ -183,7 +185,7 @@ class OracleOptimizer:
         arr, keep = self._tensor_array(grads)
         garr = (_Group * max(1, len(self.groups)))()
         for q, g in enumerate(self.groups):
-            garr[q] = _Group(g.lr, g.beta1, g.beta2, g.eps, g.weight_decay, g.step)
+            garr[q] = _Group(g.lr, g.beta1, g.beta2, g.eps, g.weight_decay, g.step, g.divisor)
         norm = ctypes.c_double()
         coef = ctypes.c_double()
         rc = lib().oracle_step(arr, len(self.params), garr, len(self.groups), float(divisor),

@@ -9,7 +9,11 @@
  * the two optimizer paragraphs "After backward, each trainable tensor has a
  * gradient ..." and "SomaSpeed batches that work across tensors ..."):
  *
- *   1. normalize every gradient for the effective batch: g / d;
+ *   1. normalize every gradient for the effective batch: g / d, where d is
+ *      the step's divisor or, if its group sets one, the group's own (the
+ *      veRL write-up divides the loss by the number of accumulated
+ *      micro-batches, 4.2 PPO Update; groups accumulated over different
+ *      counts divide by different numbers);
  *   2. measure one global L2 norm of the normalized gradients, where each
  *      owned shard counts once (non-owned, i.e. replicated, tensors do not
  *      enter the sum) and frozen tensors do not enter at all;
@@ -57,7 +61,8 @@ typedef struct {
 
 typedef struct {
     double lr, beta1, beta2, eps, weight_decay;
-    int64_t step; /* steps this group has taken so far */
+    int64_t step;   /* steps this group has taken so far */
+    double divisor; /* this group's effective-batch divisor; 0 = the step's */
 } oracle_group;
 
 /* IEEE 754 binary16 word -> exact fp64: 1 sign bit, 5 exponent bits (bias
@@ -157,7 +162,16 @@ int oracle_step(oracle_tensor *ts, int64_t n, oracle_group *groups, int32_t ngro
         if (ts[k].trainable && (ts[k].group < 0 || ts[k].group >= ngroups))
             return -1;
 
-    double norm = oracle_global_norm(ts, n, divisor);
+    /* Step 2 with each tensor normalized by its group's divisor (the step's
+     * divisor unless the group sets its own). */
+    double total = 0.0;
+    for (int64_t k = 0; k < n; ++k) {
+        if (!ts[k].trainable || !ts[k].owned)
+            continue;
+        double dk = groups[ts[k].group].divisor > 0.0 ? groups[ts[k].group].divisor : divisor;
+        total += oracle_tensor_sqsum(ts[k].grad, ts[k].grad_dtype, ts[k].numel, dk);
+    }
+    double norm = sqrt(total);
     double c = oracle_clip_coef(norm, max_norm);
 
     /* A group takes a step when it has at least one trainable tensor. */
@@ -175,7 +189,8 @@ int oracle_step(oracle_tensor *ts, int64_t n, oracle_group *groups, int32_t ngro
         const oracle_group *gp = &groups[ts[k].group];
         oracle_adamw_update(ts[k].param, ts[k].grad, ts[k].grad_dtype, ts[k].exp_avg,
                             ts[k].exp_avg_sq, ts[k].numel, gp->lr, gp->beta1, gp->beta2,
-                            gp->eps, gp->weight_decay, gp->step, c, divisor);
+                            gp->eps, gp->weight_decay, gp->step, c,
+                            gp->divisor > 0.0 ? gp->divisor : divisor);
     }
     if (norm_out)
         *norm_out = norm;

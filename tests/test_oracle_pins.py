@@ -352,3 +352,31 @@ def test_binary16_decoder_all_words():
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
     t = torch.tensor([1.0, -2.5, 6.1e-5, 65504.0], dtype=torch.float16)
     assert oracle.tensor_sqsum(t, 2.0) == sum((float(x) / 2.0) ** 2 for x in t.float())
+
+
+def test_group_divisors_match_the_library_with_pre_divided_gradients():
+    # A group's own divisor d_q normalizes its gradients before the norm and
+    # the update: the same as torch with each group's gradients divided by
+    # d_q and a step divisor of 1.
+    rng = np.random.default_rng(41)
+    sizes = (33, 64, 10, 7)
+    params = [rng.standard_normal(n) * 0.02 for n in sizes]
+    flags = [(0, True, True), (1, True, True), (1, True, False), (2, True, True)]
+    divs = (0.0, 3.0, 16.0)  # group 0 keeps the step's divisor
+    step_d = 4.0
+    groups = [GroupState(lr=1e-3, weight_decay=0.01, divisor=divs[0]),
+              GroupState(lr=2e-3, beta1=0.8, divisor=divs[1]),
+              GroupState(lr=5e-4, weight_decay=0.1, divisor=divs[2])]
+    steps = 3
+    grads = [[f32(rng.standard_normal(n)) for n in sizes] for _ in range(steps)]
+    eff = [step_d if divs[g] == 0.0 else divs[g] for g, _, _ in flags]
+    pre = [[(g.astype(np.float64) / eff[k]) for k, g in enumerate(gs)] for gs in grads]
+    ref_p, ref_m, ref_v, ref_norms = _torch_reference_run(params, pre, flags, groups, 1.0, 1.0,
+                                                          [(1e-3, 2e-3, 5e-4)] * steps)
+    opt = OracleOptimizer(params, flags, [GroupState(**vars(g)) for g in groups])
+    for s in range(steps):
+        norm, c = opt.step(grads[s], step_d, 1.0)
+        assert math.isclose(norm, ref_norms[s], rel_tol=1e-13)
+    for k in range(len(sizes)):
+        np.testing.assert_allclose(opt.params[k], ref_p[k], rtol=1e-12)
+        np.testing.assert_allclose(opt.exp_avg[k], ref_m[k], rtol=1e-11)
