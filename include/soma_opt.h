@@ -6,7 +6,8 @@
  * pace", optimizer paragraphs "After backward, each trainable tensor has a
  * gradient ..." and "SomaSpeed batches that work across tensors ..."):
  *
- *   over a list of tensors, with d = grad_divisor,
+ *   over a list of tensors, with d = grad_divisor (or the tensor's group
+ *   divisor, see soma_opt_set_group_divisor),
  *     norm = sqrt( sum over trainable, owned tensors of sum_i (g_i / d)^2 )
  *     c    = min(1, max_norm / (norm + 1e-6))
  *   then, for every element of every trainable tensor (owned or not),
@@ -129,6 +130,13 @@ soma_status_t soma_opt_get_group(soma_opt_t opt, int32_t group, double *lr, doub
 soma_status_t soma_opt_set_group(soma_opt_t opt, int32_t group, double lr, double beta1,
                                  double beta2, double eps, double weight_decay);
 
+/* A group's own effective-batch divisor: its gradients are normalized by it
+ * (in the norm and in the update) instead of the step's grad_divisor, e.g.
+ * for parameters accumulated over a different number of micro-batches.
+ * divisor > 0 and finite, or 0 to use the step's divisor (the default). */
+soma_status_t soma_opt_set_group_divisor(soma_opt_t opt, int32_t group, double divisor);
+soma_status_t soma_opt_get_group_divisor(soma_opt_t opt, int32_t group, double *divisor);
+
 /* Step count of a group (checkpoint and resume).  set: t >= 0. */
 soma_status_t soma_opt_get_group_step(soma_opt_t opt, int32_t group, int64_t *t);
 soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
@@ -151,7 +159,8 @@ soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n
  * enqueues only the two kernels, which read each group's hyperparameters and
  * step count from a table in device memory and advance the step counts there
  * (the square-sum kernel's last CTA does it, right after deriving c).
- * grad_divisor and max_norm become part of a captured graph.
+ * grad_divisor, max_norm and the group divisors become part of a captured
+ * graph.
  *
  * Rules: soma_opt_push_groups must have run once; the first call with a list
  * must happen outside capture (it builds and uploads the tables); from then

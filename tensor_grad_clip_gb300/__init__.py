@@ -172,6 +172,15 @@ class SomaOpt:
                   weight_decay: float = 0.0):
         self._check(_abi.soma_opt_set_group(self._h, group, lr, betas[0], betas[1], eps, weight_decay))
 
+    def set_group_divisor(self, group: int, divisor: float):
+        """The group's own effective-batch divisor (0 = the step's)."""
+        self._check(_abi.soma_opt_set_group_divisor(self._h, group, divisor))
+
+    def get_group_divisor(self, group: int) -> float:
+        d = ctypes.c_double()
+        self._check(_abi.soma_opt_get_group_divisor(self._h, group, ctypes.byref(d)))
+        return d.value
+
     def get_group_step(self, group: int) -> int:
         t = ctypes.c_int64()
         self._check(_abi.soma_opt_get_group_step(self._h, group, ctypes.byref(t)))

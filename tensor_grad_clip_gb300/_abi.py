@@ -89,6 +89,8 @@ SIGNATURES = {
     "soma_opt_set_lr": (soma_status_t, [soma_opt_t, _I32, _D]),
     "soma_opt_get_group": (soma_status_t, [soma_opt_t, _I32, _DP, _DP, _DP, _DP, _DP]),
     "soma_opt_set_group": (soma_status_t, [soma_opt_t, _I32, _D, _D, _D, _D, _D]),
+    "soma_opt_set_group_divisor": (soma_status_t, [soma_opt_t, _I32, _D]),
+    "soma_opt_get_group_divisor": (soma_status_t, [soma_opt_t, _I32, _DP]),
     "soma_opt_get_group_step": (soma_status_t, [soma_opt_t, _I32, _I64P]),
     "soma_opt_set_group_step": (soma_status_t, [soma_opt_t, _I32, _I64]),
     "soma_opt_step": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_tensor_t), _I64, _D, _D,

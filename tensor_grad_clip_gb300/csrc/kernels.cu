@@ -290,7 +290,10 @@ __device__ __forceinline__ GroupHp group_constants(const DevGroup& g, int64_t t)
     return h;
 }
 
-template <bool kGraph>
+// kGroupDiv: some group has its own divisor.  Each norm chunk then belongs to
+// one group, and its partial is scaled by that group's 1/d^2; otherwise the
+// partials are raw sums of g^2 and the step's d is applied to the total.
+template <bool kGraph, bool kGroupDiv>
 __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_constant__ NormArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     __shared__ int upre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
@@ -314,7 +317,14 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
             chunk_sumsq(segs, upre, spre, a0, a1);
         }
         const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
-        if (threadIdx.x == 0) a.partials[c] = (double)bs;
+        if (threadIdx.x == 0) {
+            if (kGroupDiv) {
+                const double w = a.inv_divisor[segs[0].group];
+                a.partials[c] = (double)bs * w * w;
+            } else {
+                a.partials[c] = (double)bs;
+            }
+        }
         __syncthreads();  // segs and wsum are reused by the next chunk
     }
 
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
     for (; i < n; i += B) s += __ldcg(a.partials + i);
     s = block_sum64<kNormBlock>(s, wsum64);
     if (threadIdx.x == 0) {
-        const double norm = sqrt(s) / a.divisor;
+        const double norm = kGroupDiv ? sqrt(s) : sqrt(s) / a.divisor;
         const double q = a.max_norm / (norm + 1e-6);
         const double coef = (q < 1.0 || q != q) ? q : 1.0;  // NaN propagates
         a.res->sumsq = s;
@@ -352,7 +362,7 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
         a.res->scale = (float)(coef / a.divisor);
         a.res->nonfinite = isfinite(norm) ? 0u : 1u;
         a.res->ticket = 0u;
-        if (a.sumsq_out) *a.sumsq_out = s / (a.divisor * a.divisor);
+        if (a.sumsq_out) *a.sumsq_out = kGroupDiv ? s : s / (a.divisor * a.divisor);
     }
     if (kGraph) {
         const int q = threadIdx.x;
@@ -547,9 +557,11 @@ __device__ __forceinline__ void segment_update_low(const Seg& s, const GroupHp& 
 // time (both loaded before either is used), following its segment with a
 // forward-only cursor, so small tensors keep as many loads in flight as
 // large ones.  Head and tail elements are flattened the same way.
-template <bool kGraph>
+template <bool kGraph, bool kGroupDiv>
 __device__ __forceinline__ void chunk_update(const Seg* segs, const int* vpre, const int* spre,
-                                             const UpdateArgs& a, const GroupHp* shp, float scale) {
+                                             const UpdateArgs& a, const GroupHp* shp, const float* gscale,
+                                             float scale1) {
+    auto scale_of = [&](const Seg& s) { return kGroupDiv ? gscale[s.group] : scale1; };
     const int B = blockDim.x;
     const int V = vpre[kMaxSegsPerChunk];
     int k = 0;
@@ -568,13 +580,13 @@ __device__ __forceinline__ void chunk_update(const Seg* segs, const int* vpre, c
         {
             const Seg& s = segs[k0];
             const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
-            compute8(s, x0, h, scale);
+            compute8(s, x0, h, scale_of(s));
             store8(s, v0 - vpre[k0], x0);
         }
         if (k1 >= 0) {
             const Seg& s = segs[k1];
             const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
-            compute8(s, x1, h, scale);
+            compute8(s, x1, h, scale_of(s));
             store8(s, v1 - vpre[k1], x1);
         }
     }
@@ -585,18 +597,21 @@ __device__ __forceinline__ void chunk_update(const Seg* segs, const int* vpre, c
         const Seg& s = segs[k];
         const int j = e - spre[k];
         const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
-        update_one(s, j < s.head ? j : s.head + kVec * s.nvec + (j - s.head), h, scale);
+        update_one(s, j < s.head ? j : s.head + kVec * s.nvec + (j - s.head), h, scale_of(s));
     }
 }
 
 // Chunks run in reverse list order: the gradients the square-sum kernel read
 // last are the ones most likely still in L2 when this kernel starts.
-template <bool kGraph>
+// kGroupDiv: some group sets its own divisor, so the scale c/d differs by
+// group; otherwise every element uses the one scale the norm kernel wrote.
+template <bool kGraph, bool kGroupDiv>
 __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_constant__ UpdateArgs a) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     __shared__ int vpre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
     __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
-    float scale = 0.f;
+    __shared__ float gscale[kGroupDiv ? kMaxGroups : 1];  // c / d of each group
+    float scale1 = 0.f;                                  // c / d when all groups share d
     bool ready = false;
     for (int r = blockIdx.x; r < a.t.nchunks; r += gridDim.x) {
         const int c = a.t.nchunks - 1 - r;
@@ -609,22 +624,29 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
             // scale and, for graph steps, the group constants.
             if (ns == 1) prefetch_vectors(segs[0]);
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            scale = __ldcg(&a.res->scale);
+            if (kGroupDiv) {
+                const double coef = __ldcg(&a.res->coef);
+                for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x)
+                    gscale[q] = (float)(coef / a.divisor[q]);
+            } else {
+                scale1 = __ldcg(&a.res->scale);
+            }
             if (kGraph) {
                 for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x) shp[q] = a.dhp[q];
-                __syncthreads();
             }
+            if (kGraph || kGroupDiv) __syncthreads();
             ready = true;
         }
         if (ns == 1) {
             const Seg& s = segs[0];
             const GroupHp& h = kGraph ? shp[s.group] : a.groups[s.group];
-            if (s.gdtype == kBF16) segment_update_low<kBF16>(s, h, scale);
-            else if (s.gdtype == kF16) segment_update_low<kF16>(s, h, scale);
-            else segment_update_low<kF32>(s, h, scale);
+            const float sc = kGroupDiv ? gscale[s.group] : scale1;
+            if (s.gdtype == kBF16) segment_update_low<kBF16>(s, h, sc);
+            else if (s.gdtype == kF16) segment_update_low<kF16>(s, h, sc);
+            else segment_update_low<kF32>(s, h, sc);
         } else {
             segment_prefix<false>(segs, ns, vpre, spre);
-            chunk_update<kGraph>(segs, vpre, spre, a, shp, scale);
+            chunk_update<kGraph, kGroupDiv>(segs, vpre, spre, a, shp, gscale, scale1);
         }
         __syncthreads();  // segs and the prefixes are rebuilt for the next chunk
     }
@@ -632,13 +654,16 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
 
 }  // namespace
 
-int launch_norm(const NormArgs& a, int grid, void* stream, bool graph) {
-    if (graph) norm_kernel<true><<<grid, kNormBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    else norm_kernel<false><<<grid, kNormBlock, 0, static_cast<cudaStream_t>(stream)>>>(a);
+int launch_norm(const NormArgs& a, int grid, void* stream, bool graph, bool group_div) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (graph && group_div) norm_kernel<true, true><<<grid, kNormBlock, 0, s>>>(a);
+    else if (graph) norm_kernel<true, false><<<grid, kNormBlock, 0, s>>>(a);
+    else if (group_div) norm_kernel<false, true><<<grid, kNormBlock, 0, s>>>(a);
+    else norm_kernel<false, false><<<grid, kNormBlock, 0, s>>>(a);
     return (int)cudaGetLastError();
 }
 
-int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph, bool overlap) {
+int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph, bool overlap, bool group_div) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kUpdateBlock);
@@ -649,8 +674,11 @@ int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph, bool 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    cudaError_t e = graph ? cudaLaunchKernelEx(&cfg, update_kernel<true>, a)
-                          : cudaLaunchKernelEx(&cfg, update_kernel<false>, a);
+    cudaError_t e;
+    if (graph && group_div) e = cudaLaunchKernelEx(&cfg, update_kernel<true, true>, a);
+    else if (graph) e = cudaLaunchKernelEx(&cfg, update_kernel<true, false>, a);
+    else if (group_div) e = cudaLaunchKernelEx(&cfg, update_kernel<false, true>, a);
+    else e = cudaLaunchKernelEx(&cfg, update_kernel<false, false>, a);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }

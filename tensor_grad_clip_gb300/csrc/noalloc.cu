@@ -187,6 +187,7 @@ extern "C" soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tenso
     a.res = reinterpret_cast<soma::Result*>(d);
     a.divisor = grad_divisor;
     a.max_norm = max_norm;
+    for (double& w : a.inv_divisor) w = 1.0 / grad_divisor;  // every segment is group 0 here
     if (soma::launch_norm(a, (int)std::max<int64_t>(nchunk, 1), stream) != cudaSuccess) return SOMA_ERR_CUDA;
     // norm and coef are adjacent in the result block
     if (cudaMemcpyAsync(out, d + offsetof(soma::Result, norm), 2 * sizeof(double), cudaMemcpyDefault, s) !=

@@ -60,8 +60,8 @@ struct GroupHp {
 // Written by the square-sum kernel's last CTA, read by the update kernel and
 // by soma_opt_get_norm.
 struct Result {
-    double sumsq;           // sum of g^2 over owned elements (stored gradients)
-    double norm;            // sqrt(sumsq) / d
+    double sumsq;           // sum over owned elements of g^2, or of (g / d_group)^2 with group divisors
+    double norm;            // the global norm of the normalized gradients
     double coef;            // min(1, max_norm / (norm + 1e-6))
     float scale;            // coef / d in fp32: the update multiplies g by this
     uint32_t nonfinite;     // 1 when norm is not finite
@@ -89,8 +89,9 @@ struct NormArgs {
     Table t;
     double* partials;       // one per chunk
     Result* res;
-    double divisor;
+    double divisor;         // the step's divisor (for Result::scale)
     double max_norm;
+    double inv_divisor[kMaxGroups];  // 1 / (effective divisor) of each group
     // graph-capturable step only: the last CTA advances the step count of
     // every group whose bit is set in `present` and writes its constants
     DevGroup* dgroups;
@@ -118,6 +119,7 @@ struct UpdateArgs {
     GroupHp groups[kMaxGroups];   // regular step: constants as kernel arguments
     const GroupHp* dhp;           // graph-capturable step: constants in device memory
     int32_t ngroups;
+    double divisor[kMaxGroups];   // effective divisor of each group: g' = g * (c / divisor)
 };
 
 constexpr int kNormBlock = 512;
@@ -126,11 +128,13 @@ constexpr int kUpdateBlock = 256;
 // Launch wrappers (kernels.cu).  Return the cudaError_t of the launch as int.
 // graph = true selects the variants that take group constants from device
 // memory (NormArgs::dgroups / dhp, UpdateArgs::dhp).
-int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false);
+// group_div: some group of the list sets its own divisor (NormArgs::inv_divisor).
+int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false, bool group_div = false);
 // overlap = true launches with programmatic stream serialization: the update
 // kernel may start while the previous kernel on the stream finishes, and waits
 // (griddepcontrol.wait) before it reads that kernel's results.
-int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false, bool overlap = false);
+int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false, bool overlap = false,
+                  bool group_div = false);
 int launch_finish(const FinishArgs& a, void* stream);
 
 }  // namespace soma

@@ -34,6 +34,7 @@ struct Group {
     double lr, beta1, beta2, eps, weight_decay;
     int64_t step;
     bool step_dirty;  // the host count is newer than the device table's
+    double divisor;   // the group's own effective-batch divisor; 0 = the step's
 };
 
 thread_local std::string g_create_error;
@@ -178,12 +179,14 @@ int vector_head(const uintptr_t* addr, const int* esize, int n) {
 // `chunk` elements (at most kMaxSegsPerChunk segments each).
 struct TableBuilder {
     int64_t chunk;
+    bool one_group_per_chunk;  // norm table: a chunk's partial is scaled by one group's divisor
     std::vector<soma::Seg> segs;
     std::vector<int32_t> begin{0};
     int64_t cur_elems = 0;
     int cur_segs = 0;
+    int32_t cur_group = -1;
 
-    explicit TableBuilder(int64_t c) : chunk(c) {}
+    TableBuilder(int64_t c, bool one_group) : chunk(c), one_group_per_chunk(one_group) {}
 
     void close() {
         if (cur_segs == 0) return;
@@ -198,7 +201,10 @@ struct TableBuilder {
         const int gsz = grad_size(t.grad_dtype);
         int64_t off = 0;
         while (off < n) {
-            if (cur_segs == soma::kMaxSegsPerChunk || cur_elems >= chunk) close();
+            if (cur_segs == soma::kMaxSegsPerChunk || cur_elems >= chunk ||
+                (one_group_per_chunk && cur_segs > 0 && cur_group != t.group))
+                close();
+            cur_group = t.group;
             int64_t cut = off + std::min(n - off, chunk - cur_elems);
             if (h >= 0 && cut < n && cut > h) {  // cut on the vector grid
                 cut = h + (cut - h + soma::kVec - 1) / soma::kVec * soma::kVec;
@@ -280,8 +286,8 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
         trainable_total += list[k].numel;
         if (list[k].owned) owned_total += list[k].numel;
     }
-    TableBuilder upd(chunk_size(o->update_chunk, kDefaultUpdateChunk, trainable_total, o->sm_count));
-    TableBuilder nrm(chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total, o->sm_count));
+    TableBuilder upd(chunk_size(o->update_chunk, kDefaultUpdateChunk, trainable_total, o->sm_count), false);
+    TableBuilder nrm(chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total, o->sm_count), true);
     std::vector<uint8_t> present(o->groups.size(), 0);
     int64_t trainable = 0, owned = 0;
     for (int64_t k = 0; k < n; ++k) {
@@ -478,7 +484,7 @@ soma_status_t soma_opt_add_group(soma_opt_t h, double lr, double beta1, double b
     if (st != SOMA_OK) return st;
     if ((int)o->groups.size() >= SOMA_MAX_GROUPS)
         return o->fail(SOMA_ERR_LIMIT, "at most %d parameter groups", SOMA_MAX_GROUPS);
-    o->groups.push_back(Group{lr, beta1, beta2, eps, weight_decay, 0, true});
+    o->groups.push_back(Group{lr, beta1, beta2, eps, weight_decay, 0, true, 0.0});
     *group_id = (int32_t)o->groups.size() - 1;
     return SOMA_OK;
 }
@@ -522,6 +528,25 @@ soma_status_t soma_opt_set_group(soma_opt_t h, int32_t group, double lr, double 
     return SOMA_OK;
 }
 
+soma_status_t soma_opt_set_group_divisor(soma_opt_t h, int32_t group, double divisor) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    if (!is_finite(divisor) || divisor < 0)
+        return o->fail(SOMA_ERR_INVALID_ARG, "divisor must be finite and >= 0 (got %g)", divisor);
+    o->groups[group].divisor = divisor;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_get_group_divisor(soma_opt_t h, int32_t group, double* divisor) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (group < 0 || group >= (int32_t)o->groups.size()) return o->fail(SOMA_ERR_BAD_GROUP, "group %d", group);
+    if (!divisor) return o->fail(SOMA_ERR_INVALID_ARG, "divisor is NULL");
+    *divisor = o->groups[group].divisor;
+    return SOMA_OK;
+}
+
 soma_status_t soma_opt_get_group_step(soma_opt_t h, int32_t group, int64_t* t) {
     soma_opt* o = live_handle(h);
     if (!o) return SOMA_ERR_STATE;
@@ -560,6 +585,24 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
 }
 
 namespace {
+
+// Effective divisor of every group (its own, else the step's) for the
+// kernels: 1/d for the square-sum's chunk partials, d for the update scale.
+// Does a group present in the cached list set its own divisor?
+bool any_group_divisor(const soma_opt* o) {
+    for (size_t q = 0; q < o->groups.size(); ++q)
+        if (o->groups[q].divisor > 0 && q < o->group_present.size() && o->group_present[q]) return true;
+    return false;
+}
+
+void fill_divisors(const soma_opt* o, double grad_divisor, double* inv, double* div) {
+    for (int q = 0; q < soma::kMaxGroups; ++q) {
+        const double d = (q < (int)o->groups.size() && o->groups[q].divisor > 0) ? o->groups[q].divisor
+                                                                                 : grad_divisor;
+        if (inv) inv[q] = 1.0 / d;
+        if (div) div[q] = d;
+    }
+}
 
 // Everything a step does before its launches, after the arguments were
 // checked: device, ordering after the previous step, tables for this list.
@@ -610,6 +653,8 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
     soma::UpdateArgs ua{};
     ua.t = o->upd_tab;
     ua.res = o->d_res;
+    ua.ngroups = (int32_t)o->groups.size();
+    fill_divisors(o, grad_divisor, nullptr, ua.divisor);
     std::vector<int64_t> next;
     host_group_constants(o, ua, next);
     cudaError_t e;
@@ -638,7 +683,9 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         na.res = o->d_res;
         na.divisor = grad_divisor;
         na.max_norm = max_norm;
-        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream)) != cudaSuccess)
+        fill_divisors(o, grad_divisor, na.inv_divisor, nullptr);
+        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o))) !=
+            cudaSuccess)
             return o->cuda_fail(e, "launching the square-sum kernel");
     }
     if (ev && (e = cudaEventRecord((*ev)[1], (cudaStream_t)stream)) != cudaSuccess)
@@ -646,7 +693,8 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
     // without a timing event between the two kernels, the update kernel may
     // overlap the square-sum kernel's tail
     if (o->upd_grid > 0 &&
-        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, false, ev == nullptr)) != cudaSuccess)
+        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, false, ev == nullptr,
+                                              any_group_divisor(o))) != cudaSuccess)
         return o->cuda_fail(e, "launching the update kernel");
     if (ev) {
         if ((e = cudaEventRecord((*ev)[2], (cudaStream_t)stream)) != cudaSuccess)
@@ -703,8 +751,9 @@ soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n,
     na.divisor = grad_divisor;
     na.max_norm = 1.0;
     na.sumsq_out = sumsq_out;
+    fill_divisors(o, grad_divisor, na.inv_divisor, nullptr);
     cudaError_t e;
-    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream)) != cudaSuccess)
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o))) != cudaSuccess)
         return o->cuda_fail(e, "launching the square-sum kernel");
     if ((e = cudaEventRecord(o->done, (cudaStream_t)stream)) != cudaSuccess)
         return o->cuda_fail(e, "cudaEventRecord");
@@ -772,14 +821,18 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
     na.dhp = o->d_hp;
     na.present = present;
     na.ngroups = (int32_t)o->groups.size();
+    fill_divisors(o, grad_divisor, na.inv_divisor, nullptr);
     soma::UpdateArgs ua{};
     ua.t = o->upd_tab;
     ua.res = o->d_res;
     ua.dhp = o->d_hp;
     ua.ngroups = (int32_t)o->groups.size();
-    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, true)) != cudaSuccess)
+    fill_divisors(o, grad_divisor, nullptr, ua.divisor);
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, true, any_group_divisor(o))) != cudaSuccess)
         return o->cuda_fail(e, "launching the square-sum kernel");
-    if (o->upd_grid > 0 && (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true)) != cudaSuccess)
+    if (o->upd_grid > 0 &&
+        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true, false, any_group_divisor(o))) !=
+            cudaSuccess)
         return o->cuda_fail(e, "launching the update kernel");
     o->graph_locked = true;
     if (!cap) {

@@ -138,15 +138,17 @@ class DeviceList:
 
 def make_opt(w: W.Workload, device_index=0) -> SomaOpt:
     opt = SomaOpt(device_index)
-    for g in w.groups:
+    for q, g in enumerate(w.groups):
         opt.add_group(lr=g.lr, betas=(g.beta1, g.beta2), eps=g.eps, weight_decay=g.weight_decay)
+        if g.divisor:
+            opt.set_group_divisor(q, g.divisor)
     return opt
 
 
 def make_oracle(w: W.Workload, params_cpu) -> OracleOptimizer:
     flags = [(t.group, t.trainable, t.owned) for t in w.tensors]
-    groups = [GroupState(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps, weight_decay=g.weight_decay)
-              for g in w.groups]
+    groups = [GroupState(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps, weight_decay=g.weight_decay,
+                         divisor=g.divisor) for g in w.groups]
     return OracleOptimizer([p.double().numpy().reshape(-1) for p in params_cpu], flags, groups)
 
 

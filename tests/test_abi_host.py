@@ -251,3 +251,21 @@ def test_owned_flags_count_every_entry_once():
         assert owners == (list(range(world)) if sharded[k] else [k % world])
     with pytest.raises(ValueError):
         owned_flags(5, 3, 3, sharded)
+
+
+def test_group_divisor_arguments():
+    opt = SomaOpt(0)
+    opt.add_group(lr=1e-3)
+    assert opt.get_group_divisor(0) == 0.0
+    opt.set_group_divisor(0, 3.0)
+    assert opt.get_group_divisor(0) == 3.0
+    for bad in (-1.0, float("nan"), float("inf")):
+        with pytest.raises(SomaError) as e:
+            opt.set_group_divisor(0, bad)
+        assert e.value.status == _abi.SOMA_ERR_INVALID_ARG
+    with pytest.raises(SomaError) as e:
+        opt.set_group_divisor(1, 2.0)
+    assert e.value.status == _abi.SOMA_ERR_BAD_GROUP
+    opt.set_group_divisor(0, 0.0)  # back to the step's divisor
+    assert opt.get_group_divisor(0) == 0.0
+    opt.close()

@@ -278,3 +278,18 @@ def test_fp16_grads_and_master_weight_copies(grad_dt, low_dt):
     w = _custom(tensors, groups, steps=4, grad_std=0.5)
     run_parity(w)
     run_parity(w, shift=[(1, 1, 1, 1)] * len(tensors), tuning=dict(update_chunk=1024, norm_chunk=2048))
+
+
+def test_group_divisors():
+    # Each group normalizes by its own divisor (3 is not a power of two);
+    # small chunks put several groups in one chunk.
+    T = W.TensorSpec
+    tensors = [T("a", (300, 17), W.BF16), T("b", (4099,), W.F32, group=1),
+               T("c", (77,), W.F16, group=2, owned=False), T("d", (65541,), W.BF16, group=1),
+               T("e", (9,), W.F32, group=2)]
+    groups = (W.GroupSpec(lr=1e-3, weight_decay=0.01), W.GroupSpec(lr=2e-3, divisor=3.0),
+              W.GroupSpec(lr=5e-4, weight_decay=0.1, divisor=16.0))
+    w = _custom(tensors, groups, divisor=4.0, steps=3, grad_std=2.0)
+    res = run_parity(w)
+    assert all(rc < 1.0 for _, _, _, rc in res)
+    run_parity(w, tuning=dict(update_chunk=512, norm_chunk=1024))

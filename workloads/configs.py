@@ -53,6 +53,7 @@ class GroupSpec:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.0
+    divisor: float = 0.0  # the group's own gradient divisor; 0 = the list's
 
 
 @dataclass(frozen=True)
