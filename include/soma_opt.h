@@ -70,7 +70,7 @@ typedef int32_t soma_status_t;
 #define SOMA_DTYPE_F16   2  /* IEEE binary16 */
 
 #define SOMA_MAX_GROUPS  64
-#define SOMA_ABI_VERSION 2
+#define SOMA_ABI_VERSION 3
 
 typedef struct soma_opt soma_opt;
 typedef soma_opt *soma_opt_t;
@@ -147,8 +147,9 @@ soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
  * its step count by one.  Enqueues two kernels on `stream` and returns without
  * waiting for them: the owned square-sum (which also derives norm and c on
  * the device) and the fused update.  No device-to-host synchronisation
- * happens, except that a list differing from the previous call's waits for
- * the previous step's kernels before the device tables are rewritten. */
+ * happens, except that a list the handle has not prepared yet waits for the
+ * previous step's kernels before its device tables are written (see the
+ * prepared-list cache below). */
 soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
                             double grad_divisor, double max_norm, void *stream);
 
@@ -245,6 +246,21 @@ typedef struct {
     int32_t reserved;
 } soma_plan_t;
 soma_status_t soma_opt_get_plan(soma_opt_t opt, soma_plan_t *plan);
+
+/* Prepared-list cache.  A handle keeps the device tables of the last
+ * SOMA_PLAN_CACHE distinct lists it stepped (lists compared entry by entry,
+ * bytewise), so that steps alternating between a few lists, such as two
+ * gradient buffers used in turn, find their tables ready: no validation, no
+ * host table build, no upload and no wait.  A new list replaces the least
+ * recently used one.  soma_opt_set_tuning drops them all.  The caller must
+ * not free or reuse a buffer that a prepared list names while a step on that
+ * list may still be in flight; the cache holds pointers only and never
+ * dereferences them on the host.
+ * builds: table builds so far; reuses: steps that found their list
+ * prepared; entries: lists held now.  Any pointer may be NULL. */
+#define SOMA_PLAN_CACHE 4
+soma_status_t soma_opt_get_cache_stats(soma_opt_t opt, int64_t *builds, int64_t *reuses,
+                                       int32_t *entries);
 
 /* Tuning knobs for benchmarks: elements per update chunk and per norm chunk
  * (rounded to a multiple of 64; 0 = automatic: 16 Ki / 64 Ki elements, less

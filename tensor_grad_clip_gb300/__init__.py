@@ -248,6 +248,13 @@ class SomaOpt:
         self._check(_abi.soma_opt_get_plan(self._h, ctypes.byref(p)))
         return {name: getattr(p, name) for name, _ in soma_plan_t._fields_ if name != "reserved"}
 
+    def cache_stats(self) -> dict:
+        """Prepared-list cache: table builds, steps that reused a prepared
+        list, lists held now."""
+        b, r, e = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+        self._check(_abi.soma_opt_get_cache_stats(self._h, ctypes.byref(b), ctypes.byref(r), ctypes.byref(e)))
+        return {"builds": b.value, "reuses": r.value, "entries": e.value}
+
     def set_tuning(self, update_chunk: int = 0, norm_chunk: int = 0, update_ctas_per_sm: int = 0,
                    norm_ctas_per_sm: int = 0):
         self._check(_abi.soma_opt_set_tuning(self._h, update_chunk, norm_chunk, update_ctas_per_sm,

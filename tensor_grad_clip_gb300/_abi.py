@@ -24,8 +24,9 @@ SOMA_DTYPE_F32 = 0
 SOMA_DTYPE_BF16 = 1
 SOMA_DTYPE_F16 = 2
 SOMA_MAX_GROUPS = 64
-SOMA_ABI_VERSION = 2
+SOMA_ABI_VERSION = 3
 SOMA_MAX_RANKS = 65536
+SOMA_PLAN_CACHE = 4
 
 soma_status_t = ctypes.c_int32
 soma_opt_t = ctypes.c_void_p
@@ -99,6 +100,7 @@ SIGNATURES = {
     "soma_opt_set_timing": (soma_status_t, [soma_opt_t, _I32]),
     "soma_opt_read_timing": (soma_status_t, [soma_opt_t, _DP, _DP, _I64P]),
     "soma_opt_get_plan": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_plan_t)]),
+    "soma_opt_get_cache_stats": (soma_status_t, [soma_opt_t, _I64P, _I64P, _I32P]),
     "soma_opt_set_tuning": (soma_status_t, [soma_opt_t, _I32, _I32, _I32, _I32]),
     "soma_status_string": (ctypes.c_char_p, [soma_status_t]),
     "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),

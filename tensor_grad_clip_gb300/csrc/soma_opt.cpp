@@ -1,8 +1,8 @@
 // Host side of the C ABI declared in include/soma_opt.h.
 //
-// soma_opt_step: check every argument (nothing changes on failure) -> if the
-// list differs from the previous call's, rebuild the norm and update tables
-// on the host and upload them -> derive each group's per-step constants in
+// soma_opt_step: check every argument (nothing changes on failure) -> find
+// the list among the handle's prepared lists, else build its norm and update
+// tables on the host and upload them -> derive each group's per-step constants in
 // fp64 -> enqueue the square-sum kernel, then the update kernel, on the
 // caller's stream.  The clip coefficient never leaves the device.
 #include "soma_opt.h"
@@ -29,6 +29,7 @@ constexpr int32_t kDefaultNormChunk = 65536;
 constexpr int64_t kMinAutoChunk = 1024;   // smallest chunk the automatic sizing picks
 constexpr int64_t kAutoChunksPerSm = 4;   // small lists: aim for this many chunks per SM
 constexpr size_t kTimingRing = 1024;
+constexpr int kMaxPlans = SOMA_PLAN_CACHE;
 
 struct Group {
     double lr, beta1, beta2, eps, weight_decay;
@@ -50,6 +51,20 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+// One prepared list: the entries as the caller passed them (the cache key)
+// and the device tables and launch shapes built for them.
+struct PreparedList {
+    bool valid = false;
+    uint64_t used = 0;              // stamp of the last step that ran it
+    std::vector<soma_tensor_t> key;
+    char* d_tables = nullptr;
+    size_t cap = 0;                 // bytes
+    soma::Table norm_tab{}, upd_tab{};
+    std::vector<uint8_t> group_present;
+    int norm_grid = 1, upd_grid = 0;
+    soma_plan_t info{};
+};
+
 struct soma_opt {
     int32_t device = 0;
     std::vector<Group> groups;
@@ -67,8 +82,6 @@ struct soma_opt {
     soma::Result* h_res = nullptr;  // pinned
     double* d_partials = nullptr;
     size_t partials_cap = 0;        // elements
-    char* d_tables = nullptr;
-    size_t tables_cap = 0;          // bytes
     char* h_staging = nullptr;      // pinned
     size_t staging_cap = 0;
     cudaEvent_t done = nullptr;     // recorded after each step's last kernel
@@ -82,9 +95,14 @@ struct soma_opt {
     bool groups_pushed = false;
     bool graph_locked = false;           // a graph step ran: the tables stay as they are
 
-    // the list the device tables describe
-    std::vector<soma_tensor_t> cached;
-    bool cache_valid = false;
+    // Prepared lists, each with its own device tables, so that a step
+    // alternating between a few lists (double-buffered gradients, two models
+    // on one handle) builds and uploads nothing; the least recently used one
+    // is replaced.  Below, copies of the active one's launch parameters.
+    std::array<PreparedList, kMaxPlans> plans;
+    int active = -1;
+    uint64_t stamp = 0;
+    int64_t plan_builds = 0, plan_reuses = 0;
     soma::Table norm_tab{}, upd_tab{};
     std::vector<uint8_t> group_present;
     int norm_grid = 1, upd_grid = 0;
@@ -279,6 +297,33 @@ int64_t chunk_size(int32_t requested, int32_t dflt, int64_t total, int sm_count)
     return std::max<int64_t>(kMinAutoChunk, std::min<int64_t>(dflt, spread));
 }
 
+// Makes plan i the one the next launches use.
+void activate(soma_opt* o, int i) {
+    PreparedList& pl = o->plans[i];
+    pl.used = ++o->stamp;
+    o->active = i;
+    o->norm_tab = pl.norm_tab;
+    o->upd_tab = pl.upd_tab;
+    o->group_present = pl.group_present;
+    o->norm_grid = pl.norm_grid;
+    o->upd_grid = pl.upd_grid;
+    o->plan = pl.info;
+}
+
+// Index of the prepared list equal to `list`, or -1 (the active one first).
+int find_plan(const soma_opt* o, const soma_tensor_t* list, int64_t n) {
+    auto equal = [&](const PreparedList& pl) {
+        return pl.valid && (int64_t)pl.key.size() == n &&
+               (n == 0 || std::memcmp(pl.key.data(), list, (size_t)n * sizeof(soma_tensor_t)) == 0);
+    };
+    if (o->active >= 0 && equal(o->plans[o->active])) return o->active;
+    for (int i = 0; i < kMaxPlans; ++i)
+        if (i != o->active && equal(o->plans[i])) return i;
+    return -1;
+}
+
+// Builds the tables of a list not yet prepared into a free slot, else into
+// the least recently used one, and activates it.
 soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* stream) {
     int64_t trainable_total = 0, owned_total = 0;
     for (int64_t k = 0; k < n; ++k) {
@@ -316,8 +361,16 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
     const size_t bytes = align_up(o_nb + nrm.begin.size() * sizeof(int32_t), 256);
     const size_t nparts = std::max<size_t>(1, (size_t)nrm.nchunks());
 
+    int slot = 0;
+    for (int i = 1; i < kMaxPlans && o->plans[slot].valid; ++i)
+        if (!o->plans[i].valid || o->plans[i].used < o->plans[slot].used) slot = i;
+    PreparedList& pl = o->plans[slot];
+
+    // a step in flight may still read the slot's tables, the partials or the staging buffer
     soma_status_t st = wait_idle(o);
     if (st != SOMA_OK) return st;
+    pl.valid = false;
+    if (o->active == slot) o->active = -1;
     cudaError_t e;
     if (bytes > o->staging_cap) {
         if (o->h_staging) cudaFreeHost(o->h_staging);
@@ -326,12 +379,12 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
         if ((e = cudaMallocHost(&o->h_staging, bytes)) != cudaSuccess) return o->cuda_fail(e, "cudaMallocHost(tables)");
         o->staging_cap = bytes;
     }
-    if (bytes > o->tables_cap) {
-        if (o->d_tables) cudaFree(o->d_tables);
-        o->d_tables = nullptr;
-        o->tables_cap = 0;
-        if ((e = cudaMalloc(&o->d_tables, bytes)) != cudaSuccess) return o->cuda_fail(e, "cudaMalloc(tables)");
-        o->tables_cap = bytes;
+    if (bytes > pl.cap) {
+        if (pl.d_tables) cudaFree(pl.d_tables);
+        pl.d_tables = nullptr;
+        pl.cap = 0;
+        if ((e = cudaMalloc(&pl.d_tables, bytes)) != cudaSuccess) return o->cuda_fail(e, "cudaMalloc(tables)");
+        pl.cap = bytes;
     }
     if (nparts > o->partials_cap) {
         if (o->d_partials) cudaFree(o->d_partials);
@@ -346,34 +399,37 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
     std::memcpy(h + o_ns, nrm.segs.data(), nrm.segs.size() * sizeof(soma::Seg));
     std::memcpy(h + o_ub, upd.begin.data(), upd.begin.size() * sizeof(int32_t));
     std::memcpy(h + o_nb, nrm.begin.data(), nrm.begin.size() * sizeof(int32_t));
-    if ((e = cudaMemcpyAsync(o->d_tables, h, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(pl.d_tables, h, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream)) != cudaSuccess)
         return o->cuda_fail(e, "cudaMemcpyAsync(tables)");
 
-    char* d = o->d_tables;
-    o->upd_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_us),
+    char* d = pl.d_tables;
+    pl.upd_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_us),
                              reinterpret_cast<const int32_t*>(d + o_ub), upd.nchunks()};
-    o->norm_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_ns),
+    pl.norm_tab = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_ns),
                               reinterpret_cast<const int32_t*>(d + o_nb), nrm.nchunks()};
     const int64_t ucap = o->update_ctas_per_sm > 0 ? (int64_t)o->sm_count * o->update_ctas_per_sm : INT32_MAX;
     const int64_t ncap = o->norm_ctas_per_sm > 0 ? (int64_t)o->sm_count * o->norm_ctas_per_sm : INT32_MAX;
-    o->upd_grid = (int)std::min<int64_t>(upd.nchunks(), ucap);
-    o->norm_grid = (int)std::max<int64_t>(1, std::min<int64_t>(nrm.nchunks(), ncap));
-    o->group_present = present;
-    o->cached.assign(list, list + n);
-    o->cache_valid = true;
+    pl.upd_grid = (int)std::min<int64_t>(upd.nchunks(), ucap);
+    pl.norm_grid = (int)std::max<int64_t>(1, std::min<int64_t>(nrm.nchunks(), ncap));
+    pl.group_present = present;
+    pl.key.assign(list, list + n);
 
-    soma_plan_t& p = o->plan;
+    soma_plan_t& p = pl.info;
+    p = soma_plan_t{};
     p.norm_chunks = nrm.nchunks();
     p.norm_segments = (int64_t)nrm.segs.size();
     p.update_chunks = upd.nchunks();
     p.update_segments = (int64_t)upd.segs.size();
-    p.norm_grid = o->norm_grid;
+    p.norm_grid = pl.norm_grid;
     p.norm_block = soma::kNormBlock;
-    p.update_grid = o->upd_grid;
+    p.update_grid = pl.upd_grid;
     p.update_block = soma::kUpdateBlock;
     p.trainable_numel = trainable;
     p.owned_numel = owned;
-    p.launches_per_step = 1 + (o->upd_grid > 0 ? 1 : 0);
+    p.launches_per_step = 1 + (pl.upd_grid > 0 ? 1 : 0);
+    pl.valid = true;
+    o->plan_builds += 1;
+    activate(o, slot);
     return SOMA_OK;
 }
 
@@ -403,19 +459,20 @@ soma_status_t capturing(soma_opt* o, void* stream, bool* yes) {
     return SOMA_OK;
 }
 
-// Common argument checks of the two step entry points; sets *same when the
-// list equals the cached one.
+// Common argument checks of the step entry points.  *hit: the prepared list
+// equal to `list`, or -1; only a list not prepared yet is validated entry by
+// entry (a prepared one was validated when it was built, and groups are never
+// removed).
 soma_status_t check_step_args(soma_opt* o, const soma_tensor_t* list, int64_t n, double grad_divisor,
-                              double max_norm, bool* same) {
+                              double max_norm, int* hit) {
     if (n < 0) return o->fail(SOMA_ERR_INVALID_ARG, "n < 0");
     if (n > 0 && !list) return o->fail(SOMA_ERR_INVALID_ARG, "list is NULL with n > 0");
     if (!is_finite(grad_divisor) || grad_divisor <= 0)
         return o->fail(SOMA_ERR_INVALID_ARG, "grad_divisor must be finite and > 0 (got %g)", grad_divisor);
     if (!is_finite(max_norm) || max_norm <= 0)
         return o->fail(SOMA_ERR_INVALID_ARG, "max_norm must be finite and > 0 (got %g)", max_norm);
-    *same = o->cache_valid && (int64_t)o->cached.size() == n &&
-            (n == 0 || std::memcmp(o->cached.data(), list, (size_t)n * sizeof(soma_tensor_t)) == 0);
-    if (!*same) {
+    *hit = find_plan(o, list, n);
+    if (*hit < 0) {
         for (int64_t k = 0; k < n; ++k) {
             soma_status_t st = validate_entry(o, list[k], k);
             if (st != SOMA_OK) return st;
@@ -580,7 +637,8 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
     o->norm_chunk = norm_chunk / 64 * 64;
     o->update_ctas_per_sm = update_ctas_per_sm;
     o->norm_ctas_per_sm = norm_ctas_per_sm;
-    o->cache_valid = false;
+    for (auto& pl : o->plans) pl.valid = false;
+    o->active = -1;
     return SOMA_OK;
 }
 
@@ -588,7 +646,7 @@ namespace {
 
 // Effective divisor of every group (its own, else the step's) for the
 // kernels: 1/d for the square-sum's chunk partials, d for the update scale.
-// Does a group present in the cached list set its own divisor?
+// Does a group present in the active list set its own divisor?
 bool any_group_divisor(const soma_opt* o) {
     for (size_t q = 0; q < o->groups.size(); ++q)
         if (o->groups[q].divisor > 0 && q < o->group_present.size() && o->group_present[q]) return true;
@@ -606,7 +664,7 @@ void fill_divisors(const soma_opt* o, double grad_divisor, double* inv, double* 
 
 // Everything a step does before its launches, after the arguments were
 // checked: device, ordering after the previous step, tables for this list.
-soma_status_t prepare(soma_opt* o, const soma_tensor_t* list, int64_t n, bool same, void* stream) {
+soma_status_t prepare(soma_opt* o, const soma_tensor_t* list, int64_t n, int hit, void* stream) {
     soma_status_t st = ensure_device(o);
     if (st != SOMA_OK) return st;
     cudaError_t e;
@@ -615,11 +673,12 @@ soma_status_t prepare(soma_opt* o, const soma_tensor_t* list, int64_t n, bool sa
         if ((e = cudaStreamWaitEvent((cudaStream_t)stream, o->done, 0)) != cudaSuccess)
             return o->cuda_fail(e, "cudaStreamWaitEvent");
     }
-    if (!same) {
-        o->cache_valid = false;
-        if ((st = rebuild(o, list, n, stream)) != SOMA_OK) return st;
+    if (hit >= 0) {
+        activate(o, hit);
+        o->plan_reuses += 1;
+        return SOMA_OK;
     }
-    return SOMA_OK;
+    return rebuild(o, list, n, stream);
 }
 
 // Per-group constants of the next step (fp64 on the host, rounded once) and
@@ -718,15 +777,14 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
                             double max_norm, void* stream) {
     soma_opt* o = live_handle(h);
     if (!o) return SOMA_ERR_STATE;
-    // An unchanged list was validated when it was cached (groups are never removed).
-    bool same = false;
-    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    int hit = -1;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &hit);
     if (st != SOMA_OK) return st;
-    if (!same && o->graph_locked)
+    if (o->graph_locked && hit != o->active)
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
-    if ((st = prepare(o, list, n, same, stream)) != SOMA_OK) return st;
+    if ((st = prepare(o, list, n, hit, stream)) != SOMA_OK) return st;
     return launch_step(o, grad_divisor, max_norm, nullptr, 0, stream);
 }
 
@@ -736,14 +794,14 @@ soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n,
     if (!o) return SOMA_ERR_STATE;
     if (!sumsq_out || (uintptr_t)sumsq_out % alignof(double) != 0)
         return o->fail(SOMA_ERR_INVALID_ARG, "sumsq_out must be a non-null, 8-byte aligned device pointer");
-    bool same = false;
-    soma_status_t st = check_step_args(o, list, n, grad_divisor, 1.0, &same);
+    int hit = -1;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, 1.0, &hit);
     if (st != SOMA_OK) return st;
-    if (!same && o->graph_locked)
+    if (o->graph_locked && hit != o->active)
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
-    if ((st = prepare(o, list, n, same, stream)) != SOMA_OK) return st;
+    if ((st = prepare(o, list, n, hit, stream)) != SOMA_OK) return st;
     soma::NormArgs na{};
     na.t = o->norm_tab;
     na.partials = o->d_partials;
@@ -771,14 +829,14 @@ soma_status_t soma_opt_step_from_sumsq(soma_opt_t h, const soma_tensor_t* list, 
         return o->fail(SOMA_ERR_INVALID_ARG, "rank_sumsq must be a non-null, 8-byte aligned device pointer");
     if (nranks < 1 || nranks > SOMA_MAX_RANKS)
         return o->fail(SOMA_ERR_INVALID_ARG, "nranks must be in [1, %d]", SOMA_MAX_RANKS);
-    bool same = false;
-    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    int hit = -1;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &hit);
     if (st != SOMA_OK) return st;
-    if (!same && o->graph_locked)
+    if (o->graph_locked && hit != o->active)
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
-    if ((st = prepare(o, list, n, same, stream)) != SOMA_OK) return st;
+    if ((st = prepare(o, list, n, hit, stream)) != SOMA_OK) return st;
     return launch_step(o, grad_divisor, max_norm, rank_sumsq, nranks, stream);
 }
 
@@ -786,16 +844,16 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
                                   double max_norm, void* stream) {
     soma_opt* o = live_handle(h);
     if (!o) return SOMA_ERR_STATE;
-    bool same = false;
-    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &same);
+    int hit = -1;
+    soma_status_t st = check_step_args(o, list, n, grad_divisor, max_norm, &hit);
     if (st != SOMA_OK) return st;
-    if (!same && o->graph_locked)
+    if (o->graph_locked && hit != o->active)
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
     bool cap = false;
     if ((st = capturing(o, stream, &cap)) != SOMA_OK) return st;
-    if (cap && (!o->dev_ready || !same))
+    if (cap && (!o->dev_ready || hit < 0 || hit != o->active))
         return o->fail(SOMA_ERR_STATE, "run soma_opt_step_graph once with this list before capturing it");
     if (!o->groups_pushed)
         return o->fail(SOMA_ERR_STATE, "soma_opt_push_groups must run before the first graph-capturable step");
@@ -804,9 +862,11 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
     if (!cap && o->have_done && o->last_stream != stream &&
         (e = cudaStreamWaitEvent((cudaStream_t)stream, o->done, 0)) != cudaSuccess)
         return o->cuda_fail(e, "cudaStreamWaitEvent");
-    if (!same) {
-        o->cache_valid = false;
-        if ((st = rebuild(o, list, n, stream)) != SOMA_OK) return st;
+    if (hit >= 0) {
+        activate(o, hit);
+        o->plan_reuses += 1;
+    } else if ((st = rebuild(o, list, n, stream)) != SOMA_OK) {
+        return st;
     }
     uint64_t present = 0;
     for (size_t q = 0; q < o->group_present.size(); ++q)
@@ -981,6 +1041,19 @@ soma_status_t soma_opt_get_plan(soma_opt_t h, soma_plan_t* plan) {
     return SOMA_OK;
 }
 
+soma_status_t soma_opt_get_cache_stats(soma_opt_t h, int64_t* builds, int64_t* reuses, int32_t* entries) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (builds) *builds = o->plan_builds;
+    if (reuses) *reuses = o->plan_reuses;
+    if (entries) {
+        int32_t k = 0;
+        for (const auto& pl : o->plans) k += pl.valid ? 1 : 0;
+        *entries = k;
+    }
+    return SOMA_OK;
+}
+
 void soma_opt_destroy(soma_opt_t h) {
     soma_opt* o = live_handle(h);
     if (!o) return;
@@ -997,7 +1070,8 @@ void soma_opt_destroy(soma_opt_t h) {
         if (o->done) cudaEventDestroy(o->done);
         if (o->d_res) cudaFree(o->d_res);
         if (o->d_partials) cudaFree(o->d_partials);
-        if (o->d_tables) cudaFree(o->d_tables);
+        for (auto& pl : o->plans)
+            if (pl.d_tables) cudaFree(pl.d_tables);
         if (o->d_groups) cudaFree(o->d_groups);
         if (o->d_hp) cudaFree(o->d_hp);
         if (o->h_res) cudaFreeHost(o->h_res);

@@ -269,3 +269,23 @@ def test_group_divisor_arguments():
     opt.set_group_divisor(0, 0.0)  # back to the step's divisor
     assert opt.get_group_divisor(0) == 0.0
     opt.close()
+
+
+def test_header_constants_match_the_binding():
+    text = open(HEADER).read()
+    defs = {k: v.strip() for k, v in re.findall(r"#define\s+(SOMA_\w+)[ \t]+([^/\n]+)", text)}
+    for name, value in defs.items():
+        if name.endswith("_H") or not hasattr(_abi, name):
+            continue
+        assert eval(value.replace("u", "")) == getattr(_abi, name), name
+    assert "SOMA_PLAN_CACHE" in defs and "SOMA_ABI_VERSION" in defs
+
+
+def test_cache_stats_of_a_fresh_handle_and_after_a_failed_step():
+    opt = SomaOpt(0)
+    opt.add_group(lr=1e-3)
+    assert opt.cache_stats() == {"builds": 0, "reuses": 0, "entries": 0}
+    assert _step(opt, [_entry(grad_dtype=9)]) == _abi.SOMA_ERR_DTYPE
+    assert opt.cache_stats() == {"builds": 0, "reuses": 0, "entries": 0}
+    assert _abi.soma_opt_get_cache_stats(opt.handle, None, None, None) == _abi.SOMA_OK
+    opt.close()

@@ -245,6 +245,8 @@ def test_list_change_rebuilds_tables():
                 # the oracles stepped 3 times each, so only m (no bias correction) matches
                 assert_close("m", d.m[k].cpu().numpy(), o.exp_avg[k])
     assert opt.get_group_step(0) == 6
+    # both lists stay prepared: two table builds, four steps that reused one
+    assert opt.cache_stats() == {"builds": 2, "reuses": 4, "entries": 2}
     opt.close()
 
 
@@ -293,3 +295,29 @@ def test_group_divisors():
     res = run_parity(w)
     assert all(rc < 1.0 for _, _, _, rc in res)
     run_parity(w, tuning=dict(update_chunk=512, norm_chunk=1024))
+
+
+def test_degenerate_hyperparameters():
+    # lr = 0 leaves the weights bit-unchanged (decay factor exactly 1, step
+    # size exactly 0) while the moments still advance; beta1 = beta2 = 0
+    # makes m = g' and v = g'^2 with bias corrections of exactly 1; a large
+    # eps dominates sqrt(v).
+    T = W.TensorSpec
+    tensors = [T("frozen_lr", (4099,), W.BF16), T("b0", (3001,), W.F32, group=1),
+               T("eps", (777,), W.F16, group=2), T("frozen_lr_rep", (65,), W.F32, owned=False)]
+    groups = (W.GroupSpec(lr=0.0, weight_decay=0.5), W.GroupSpec(lr=1e-3, beta1=0.0, beta2=0.0, weight_decay=0.01),
+              W.GroupSpec(lr=1e-2, eps=1.0))
+    w = _custom(tensors, groups, steps=3, grad_std=0.3)
+    run_parity(w)
+    params = W.draw_params(w, "cpu")
+    dl = DeviceList(w, params)
+    opt = make_opt(w)
+    before = [p.clone() for p in dl.p]
+    for s in (1, 2):
+        dl.load_grads(W.draw_grads(w, s, "cpu"))
+        opt.step(dl.tl, w.grad_divisor, w.max_norm)
+    torch.cuda.synchronize()
+    for k in (0, 3):
+        assert torch.equal(before[k].view(torch.int32), dl.p[k].view(torch.int32))
+        assert dl.m[k].abs().max().item() > 0
+    opt.close()
