@@ -51,8 +51,6 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="action_expert")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--copy-streams", type=int, default=1,
-                    help="streams the end-to-end run splits each step's host-to-device copy over")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tuning", default="",
@@ -216,6 +214,63 @@ def cpu_baseline(w, budget_s=10.0):
                       f"(norm + update) in {el:.1f} s, fp64, one thread"}
 
 
+def cpu_baseline_all_cores(w, budget_s=10.0):
+    """The same oracle functions on every host core: the step's two passes
+    (square-sums, then the update) split into slices of at most 1 Mi
+    elements and run on a thread pool (ctypes releases the GIL during each
+    call); square-sums are added in list order on one thread, as in the
+    oracle's own step."""
+    import concurrent.futures as cf
+    import math
+
+    import numpy as np
+
+    import oracle
+    import workloads as W
+    oracle.lib()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    idx, n = [], 0
+    for k, t in enumerate(w.tensors):
+        if t.trainable and n < 17_000_000:
+            idx.append(k)
+            n += t.numel
+    slices = []  # (p, g, m, v, group, owned) per slice, p/m/v fp64 views
+    for k in idx:
+        t = w.tensors[k]
+        p = W.draw_param(w, k, "cpu").double().numpy().reshape(-1).copy()
+        g = W.draw_grad(w, k, 1, "cpu").reshape(-1)
+        m, v = np.zeros_like(p), np.zeros_like(p)
+        for lo in range(0, t.numel, 1 << 20):
+            hi = min(t.numel, lo + (1 << 20))
+            slices.append((p[lo:hi], g[lo:hi], m[lo:hi], v[lo:hi], t.group, t.owned))
+    steps = [0] * len(w.groups)
+
+    def one_step(pool):
+        sq = list(pool.map(lambda s: oracle.tensor_sqsum(s[1], w.grad_divisor) if s[5] else 0.0, slices))
+        c = oracle.clip_coef(math.sqrt(sum(sq)), w.max_norm)
+        for q in {s[4] for s in slices}:
+            steps[q] += 1
+
+        def upd(s):
+            g = w.groups[s[4]]
+            oracle.adamw_update(s[0], s[1], s[2], s[3], lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                                weight_decay=g.weight_decay, step=steps[s[4]], c=c, divisor=w.grad_divisor)
+        list(pool.map(upd, slices))
+
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        one_step(pool)  # warm-up
+        count, t0 = 0, time.perf_counter()
+        while True:
+            one_step(pool)
+            count += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    return {"value": n * count / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(idx)} tensors ({n:,} params) of {w.name} in {len(slices)} slices, {count} steps "
+                      f"(square-sums, then update) in {el:.1f} s, fp64, {cores} threads"}
+
+
 def run_reference(args):
     """The oracle as the reference arm: K timed steps after W warm-ups, each
     a bounded sample of the workload, sized to finish within minutes."""
@@ -267,6 +322,105 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def e2e_runs(args, w, fb, tl, step_on, stream, device, barrier, world):
+    """The step through the public API with the gradients arriving from
+    pinned host memory every step, timed twice:
+
+    - pipelined (the reported value): two device gradient buffers used in
+      turn.  Step t+1's upload runs on a copy stream while step t's kernels
+      run; each step waits only for its own upload, and an upload waits for
+      the step that last read its buffer.  The handle keeps both lists
+      prepared, so switching between them costs nothing on the host.
+    - serial: one buffer; copy, step and norm read strictly in sequence.
+
+    Each step's norm is read back (a device-to-host copy and a wait) before
+    the next step is enqueued; only the next upload is already queued then."""
+    import torch
+    import torch.distributed as dist
+    from tensor_grad_clip_gb300 import TensorList
+    G = fb.G
+    host_g = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+    host_g.copy_(G)
+    G2 = G.clone()
+    tl2 = TensorList(fb.p, [G2[fb.offsets[k]:fb.offsets[k] + t.numel] for k, t in enumerate(w.tensors)], fb.m,
+                     fb.v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
+                     owned=[t.owned for t in w.tensors], params_lowp=fb.plow)
+    bufs = [(G, tl), (G2, tl2)]
+    cs = torch.cuda.Stream(device)
+    copied = [torch.cuda.Event() for _ in bufs]
+    freed = [torch.cuda.Event() for _ in bufs]
+    torch.cuda.synchronize()
+
+    def upload(t):
+        b = t % 2
+        cs.wait_event(freed[b])  # the step that last read buffer b has finished
+        with torch.cuda.stream(cs):
+            bufs[b][0].copy_(host_g, non_blocking=True)
+        copied[b].record(cs)
+
+    def pipelined(n):
+        cs.wait_stream(stream)
+        upload(0)
+        for t in range(n):
+            b = t % 2
+            stream.wait_event(copied[b])
+            opt = step_on(bufs[b][1])
+            freed[b].record(stream)
+            if t + 1 < n:
+                upload(t + 1)
+            opt.get_norm(stream)
+
+    def serial(n):
+        for _ in range(n):
+            cs.wait_stream(stream)
+            upload(0)
+            stream.wait_event(copied[0])
+            opt = step_on(tl)
+            freed[0].record(stream)
+            opt.get_norm(stream)
+
+    def timed(fn, n):
+        fn(2)  # warm-up: both lists prepared
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        fn(n)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
+        if world > 1:
+            x = torch.tensor([ms], device=device, dtype=torch.float64)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            ms = float(x.item())
+        return ms
+
+    # the host link on its own: one gradient upload, no kernels
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(cs)
+    with torch.cuda.stream(cs):
+        for _ in range(5):
+            G2.copy_(host_g, non_blocking=True)
+    l1.record(cs)
+    torch.cuda.synchronize()
+    link_gbs = 5 * G.numel() * G.element_size() / (l0.elapsed_time(l1) / 1e3) / 1e9
+    G2.copy_(G)
+
+    n = args.e2e_steps
+    elems = w.trainable_numel * world
+    p_ms = timed(pipelined, n)
+    s_ms = timed(serial, n)
+    return {"value": elems * n / (p_ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": 48,
+            "steps": n, "ms_per_step": p_ms / n,
+            "mode": "pipelined: two device gradient buffers, upload of step t+1 overlaps step t",
+            "h2d_link_gbs": link_gbs,
+            "serial": {"value": elems * n / (s_ms / 1e3), "ms_per_step": s_ms / n}}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -298,11 +452,15 @@ def run_ours(args):
         from tensor_grad_clip_gb300.sharded import ShardedStep
         sharded_step = ShardedStep(opt)
 
-    def one_step():
+    def step_on(lst):
         if sharded_step is not None:
-            sharded_step(tl, w.grad_divisor, w.max_norm)
+            sharded_step(lst, w.grad_divisor, w.max_norm)
         else:
-            opt.step(tl, w.grad_divisor, w.max_norm, stream)
+            opt.step(lst, w.grad_divisor, w.max_norm, stream)
+        return opt
+
+    def one_step():
+        step_on(tl)
 
     torch.cuda.synchronize()
 
@@ -397,57 +555,16 @@ def run_ours(args):
                                 "avg_launch_ms": norm_avg_ms, "algorithmic_bytes_per_launch": norm_bytes}}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and graph is None:
         # End to end through the C ABI: every step copies that step's gradients
-        # from pinned host memory and reads the norm back.
-        G = fb.G
-        host_g = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
-        host_g.copy_(G)
-        torch.cuda.synchronize()
-        # each step's gradients arrive in pieces over several copy streams
-        # (several copy engines); the step waits for all of them
-        ncs = max(1, args.copy_streams)
-        copy_streams = [torch.cuda.Stream(device) for _ in range(ncs)]
-        bounds = [G.numel() * j // (2 * ncs) for j in range(2 * ncs + 1)]
-        pieces = [(G[a:b], host_g[a:b]) for a, b in zip(bounds, bounds[1:])]
-
-        def upload():
-            for j, (dst, src) in enumerate(pieces):
-                cs = copy_streams[j % ncs]
-                cs.wait_stream(stream)  # the previous step no longer reads these gradients
-                with torch.cuda.stream(cs):
-                    dst.copy_(src, non_blocking=True)
-            for cs in copy_streams:
-                stream.wait_stream(cs)
-
-        for _ in range(2):
-            upload()
-            one_step()
-            opt.get_norm(stream)
-        barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            upload()
-            one_step()
-            opt.get_norm(stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        wall = time.perf_counter() - t0
-        e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": elems * world * args.e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": 48,
-               "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps, "copy_streams": ncs}
+        # from pinned host memory into a device gradient buffer, runs the step
+        # and reads the norm back to the host.
+        e2e = e2e_runs(args, w, fb, tl, step_on, stream, device, barrier, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
+        cpu["all_cores"] = cpu_baseline_all_cores(w)
 
     if rank == 0:
         line = {
