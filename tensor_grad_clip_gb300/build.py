@@ -49,7 +49,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if not force and not ptxas_info and up_to_date():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
-    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-Wall",
+    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-Wall,-ffp-contract=off",
               "-I", INCLUDE, "-I", CSRC] + ARCH
     if ptxas_info:
         common += ["-Xptxas", "-v"]

@@ -273,21 +273,10 @@ __device__ __forceinline__ void chunk_sumsq(const Seg* segs, const int* upre, co
     }
 }
 
-// Step constants of one group at step t, in fp64 rounded once to fp32 (the
-// same arithmetic as the host path of the regular step).
-__device__ __forceinline__ GroupHp group_constants(const DevGroup& g, int64_t t) {
-    const double bc1 = 1.0 - pow(g.beta1, (double)t);
-    const double bc2 = 1.0 - pow(g.beta2, (double)t);
-    GroupHp h;
-    h.decay = (float)(1.0 - g.lr * g.weight_decay);
-    h.beta1 = (float)g.beta1;
-    h.one_minus_beta1 = (float)(1.0 - g.beta1);
-    h.beta2 = (float)g.beta2;
-    h.one_minus_beta2 = (float)(1.0 - g.beta2);
-    h.step_size = (float)(g.lr / bc1);
-    h.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
-    h.eps = (float)g.eps;
-    return h;
+// Step constants of one group at step t: the same fp64 arithmetic, rounded
+// the same way, as the host derivation of a regular step.
+__device__ __noinline__ GroupHp group_constants(const DevGroup& g, int64_t t) {
+    return make_group_hp(g.lr, g.beta1, g.beta2, g.eps, g.weight_decay, t);
 }
 
 // kGroupDiv: some group has its own divisor.  Each norm chunk then belongs to
@@ -305,7 +294,21 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
     // has started; it waits for this grid's results before using them.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    for (int c = blockIdx.x; c < a.t.nchunks; c += gridDim.x) {
+    // Graph steps: CTA 0 advances the step counts and derives the group
+    // constants (they do not depend on the norm), alongside the chunk CTAs
+    // rather than after the reduction.
+    if (kGraph && blockIdx.x == 0) {
+        for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x) {
+            if ((a.present >> q) & 1ull) {
+                const int64_t t = a.dgroups[q].step + 1;
+                a.dgroups[q].step = t;
+                a.dhp[q] = group_constants(a.dgroups[q], t);
+            }
+        }
+    }
+    const int first = kGraph ? (int)blockIdx.x - 1 : (int)blockIdx.x;
+    const int stride = kGraph ? (int)gridDim.x - 1 : (int)gridDim.x;
+    for (int c = first; c >= 0 && c < a.t.nchunks; c += stride) {
         const int ns = stage_segments(a.t, c, segs);
         float a0 = 0.f, a1 = 0.f;
         if (ns == 1) {
@@ -363,14 +366,13 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
         a.res->nonfinite = isfinite(norm) ? 0u : 1u;
         a.res->ticket = 0u;
         if (a.sumsq_out) *a.sumsq_out = kGroupDiv ? s : s / (a.divisor * a.divisor);
+        wsum64[0] = coef;
     }
-    if (kGraph) {
-        const int q = threadIdx.x;
-        if (q < a.ngroups && ((a.present >> q) & 1ull)) {
-            const int64_t t = a.dgroups[q].step + 1;
-            a.dgroups[q].step = t;
-            a.dhp[q] = group_constants(a.dgroups[q], t);
-        }
+    if (kGroupDiv) {
+        __syncthreads();
+        const double coef = wsum64[0];
+        for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x)
+            a.gscale[q] = (float)(coef * a.inv_divisor[q]);
     }
 }
 
@@ -388,6 +390,8 @@ __global__ void finish_kernel(const __grid_constant__ FinishArgs a) {
     a.res->coef = coef;
     a.res->scale = (float)(coef / a.divisor);
     a.res->nonfinite = isfinite(norm) ? 0u : 1u;
+    if (a.gscale)
+        for (int q = 0; q < a.ngroups && q < kMaxGroups; ++q) a.gscale[q] = (float)(coef * a.inv_divisor[q]);
 }
 
 // ---- fused update --------------------------------------------------------
@@ -625,9 +629,8 @@ __global__ void __launch_bounds__(kUpdateBlock) update_kernel(const __grid_const
             if (ns == 1) prefetch_vectors(segs[0]);
             asm volatile("griddepcontrol.wait;" ::: "memory");
             if (kGroupDiv) {
-                const double coef = __ldcg(&a.res->coef);
                 for (int q = threadIdx.x; q < a.ngroups && q < kMaxGroups; q += blockDim.x)
-                    gscale[q] = (float)(coef / a.divisor[q]);
+                    gscale[q] = __ldcg(a.gscale + q);
             } else {
                 scale1 = __ldcg(&a.res->scale);
             }

@@ -20,6 +20,7 @@
 // cannot all be aligned at one element is processed one element at a time.
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 
 namespace soma {
@@ -46,8 +47,7 @@ struct Seg {                // 64 bytes
 };
 static_assert(sizeof(Seg) == 64, "Seg layout");
 
-// Per-group constants of one step, derived on the host in fp64 and rounded
-// once to fp32.
+// Per-group constants of one step, derived in fp64 and rounded once to fp32.
 struct GroupHp {
     float decay;            // 1 - lr * weight_decay
     float beta1, one_minus_beta1;
@@ -56,6 +56,58 @@ struct GroupHp {
     float inv_sqrt_bc2;     // 1 / sqrt(1 - beta2^t)
     float eps;
 };
+
+// fp64 operations rounded to nearest one at a time (never fused into an
+// FMA), so that the host, for regular steps, and the device, for graph
+// steps, derive the same constants bit for bit.
+#if defined(__CUDA_ARCH__)
+#define SOMA_HD __host__ __device__
+#define SOMA_DMUL(a, b) __dmul_rn(a, b)
+#define SOMA_DSUB(a, b) __dsub_rn(a, b)
+#define SOMA_DDIV(a, b) __ddiv_rn(a, b)
+#define SOMA_DSQRT(a) __dsqrt_rn(a)
+#elif defined(__CUDACC__)
+#define SOMA_HD __host__ __device__
+#define SOMA_DMUL(a, b) ((a) * (b))
+#define SOMA_DSUB(a, b) ((a) - (b))
+#define SOMA_DDIV(a, b) ((a) / (b))
+#define SOMA_DSQRT(a) sqrt(a)
+#else
+#define SOMA_HD
+#define SOMA_DMUL(a, b) ((a) * (b))
+#define SOMA_DSUB(a, b) ((a) - (b))
+#define SOMA_DDIV(a, b) ((a) / (b))
+#define SOMA_DSQRT(a) sqrt(a)
+#endif
+
+// b^t for an integer t >= 0 by repeated squaring: at most 2 log2(t) + 1
+// multiplies (fp64 transcendental functions are slow on this GPU).
+SOMA_HD inline double pow_step(double b, int64_t t) {
+    double r = 1.0;
+    while (t > 0) {
+        if (t & 1) r = SOMA_DMUL(r, b);
+        b = SOMA_DMUL(b, b);
+        t >>= 1;
+    }
+    return r;
+}
+
+// Constants of a group at step t (bias corrections 1 - beta^t of AdamW).
+SOMA_HD inline GroupHp make_group_hp(double lr, double beta1, double beta2, double eps, double weight_decay,
+                                     int64_t t) {
+    const double bc1 = SOMA_DSUB(1.0, pow_step(beta1, t));
+    const double bc2 = SOMA_DSUB(1.0, pow_step(beta2, t));
+    GroupHp h;
+    h.decay = (float)SOMA_DSUB(1.0, SOMA_DMUL(lr, weight_decay));
+    h.beta1 = (float)beta1;
+    h.one_minus_beta1 = (float)SOMA_DSUB(1.0, beta1);
+    h.beta2 = (float)beta2;
+    h.one_minus_beta2 = (float)SOMA_DSUB(1.0, beta2);
+    h.step_size = (float)SOMA_DDIV(lr, bc1);
+    h.inv_sqrt_bc2 = (float)SOMA_DDIV(1.0, SOMA_DSQRT(bc2));
+    h.eps = (float)eps;
+    return h;
+}
 
 // Written by the square-sum kernel's last CTA, read by the update kernel and
 // by soma_opt_get_norm.
@@ -92,8 +144,11 @@ struct NormArgs {
     double divisor;         // the step's divisor (for Result::scale)
     double max_norm;
     double inv_divisor[kMaxGroups];  // 1 / (effective divisor) of each group
-    // graph-capturable step only: the last CTA advances the step count of
-    // every group whose bit is set in `present` and writes its constants
+    // group divisors only: the last CTA writes c / d of each group here
+    float* gscale;
+    // graph-capturable step only: CTA 0 (launched in addition to the chunk
+    // CTAs) advances the step count of every group whose bit is set in
+    // `present` and writes its constants
     DevGroup* dgroups;
     GroupHp* dhp;
     uint64_t present;
@@ -111,6 +166,10 @@ struct FinishArgs {
     Result* res;
     double divisor;
     double max_norm;
+    // group divisors only: gscale[q] = c / d_q for q < ngroups
+    float* gscale;
+    int32_t ngroups;
+    double inv_divisor[kMaxGroups];
 };
 
 struct UpdateArgs {
@@ -119,7 +178,7 @@ struct UpdateArgs {
     GroupHp groups[kMaxGroups];   // regular step: constants as kernel arguments
     const GroupHp* dhp;           // graph-capturable step: constants in device memory
     int32_t ngroups;
-    double divisor[kMaxGroups];   // effective divisor of each group: g' = g * (c / divisor)
+    const float* gscale;          // group divisors: c / d of each group, written by the norm side
 };
 
 constexpr int kNormBlock = 512;

@@ -89,6 +89,7 @@ struct soma_opt {
     void* last_stream = nullptr;
     soma::DevGroup* d_groups = nullptr;  // graph-capturable step: group table
     soma::GroupHp* d_hp = nullptr;       // and the constants of the current step
+    float* d_gscale = nullptr;           // group divisors: c / d of each group, per step
     soma::DevGroup* h_groups = nullptr;  // pinned staging of the group table
     cudaEvent_t groups_copied = nullptr; // last copy through h_groups finished
     bool groups_copy_pending = false;
@@ -267,6 +268,8 @@ soma_status_t ensure_device(soma_opt* o) {
         return o->cuda_fail(e, "cudaEventCreate");
     if ((e = cudaMalloc(&o->d_groups, soma::kMaxGroups * sizeof(soma::DevGroup))) != cudaSuccess)
         return o->cuda_fail(e, "cudaMalloc(groups)");
+    if ((e = cudaMalloc(&o->d_gscale, soma::kMaxGroups * sizeof(float))) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMalloc(group scales)");
     if ((e = cudaMalloc(&o->d_hp, soma::kMaxGroups * sizeof(soma::GroupHp))) != cudaSuccess)
         return o->cuda_fail(e, "cudaMalloc(group constants)");
     if ((e = cudaMemset(o->d_groups, 0, soma::kMaxGroups * sizeof(soma::DevGroup))) != cudaSuccess ||
@@ -644,8 +647,6 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
 
 namespace {
 
-// Effective divisor of every group (its own, else the step's) for the
-// kernels: 1/d for the square-sum's chunk partials, d for the update scale.
 // Does a group present in the active list set its own divisor?
 bool any_group_divisor(const soma_opt* o) {
     for (size_t q = 0; q < o->groups.size(); ++q)
@@ -653,12 +654,14 @@ bool any_group_divisor(const soma_opt* o) {
     return false;
 }
 
-void fill_divisors(const soma_opt* o, double grad_divisor, double* inv, double* div) {
+// 1 / (effective divisor) of every group, its own or else the step's: the
+// square-sum scales each chunk partial by its square, and c times it is the
+// group's update scale.
+void fill_divisors(const soma_opt* o, double grad_divisor, double* inv) {
     for (int q = 0; q < soma::kMaxGroups; ++q) {
         const double d = (q < (int)o->groups.size() && o->groups[q].divisor > 0) ? o->groups[q].divisor
                                                                                  : grad_divisor;
-        if (inv) inv[q] = 1.0 / d;
-        if (div) div[q] = d;
+        inv[q] = 1.0 / d;
     }
 }
 
@@ -681,8 +684,8 @@ soma_status_t prepare(soma_opt* o, const soma_tensor_t* list, int64_t n, int hit
     return rebuild(o, list, n, stream);
 }
 
-// Per-group constants of the next step (fp64 on the host, rounded once) and
-// the step counts it will reach.
+// Per-group constants of the next step (fp64, rounded once; the graph step
+// derives the same bits on the device) and the step counts it will reach.
 void host_group_constants(soma_opt* o, soma::UpdateArgs& ua, std::vector<int64_t>& next) {
     next.assign(o->groups.size(), 0);
     for (size_t q = 0; q < o->groups.size(); ++q) {
@@ -690,18 +693,7 @@ void host_group_constants(soma_opt* o, soma::UpdateArgs& ua, std::vector<int64_t
         const bool on = q < o->group_present.size() && o->group_present[q];
         next[q] = g.step + (on ? 1 : 0);
         if (!on) continue;
-        const double t = (double)next[q];
-        const double bc1 = 1.0 - std::pow(g.beta1, t);
-        const double bc2 = 1.0 - std::pow(g.beta2, t);
-        soma::GroupHp& hp = ua.groups[q];
-        hp.decay = (float)(1.0 - g.lr * g.weight_decay);
-        hp.beta1 = (float)g.beta1;
-        hp.one_minus_beta1 = (float)(1.0 - g.beta1);
-        hp.beta2 = (float)g.beta2;
-        hp.one_minus_beta2 = (float)(1.0 - g.beta2);
-        hp.step_size = (float)(g.lr / bc1);
-        hp.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
-        hp.eps = (float)g.eps;
+        ua.groups[q] = soma::make_group_hp(g.lr, g.beta1, g.beta2, g.eps, g.weight_decay, next[q]);
     }
 }
 
@@ -713,7 +705,7 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
     ua.t = o->upd_tab;
     ua.res = o->d_res;
     ua.ngroups = (int32_t)o->groups.size();
-    fill_divisors(o, grad_divisor, nullptr, ua.divisor);
+    ua.gscale = o->d_gscale;
     std::vector<int64_t> next;
     host_group_constants(o, ua, next);
     cudaError_t e;
@@ -732,7 +724,17 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
             return o->cuda_fail(e, "cudaEventRecord");
     }
     if (rank_sums) {
-        soma::FinishArgs fa{rank_sums, nranks, o->d_res, grad_divisor, max_norm};
+        soma::FinishArgs fa{};
+        fa.parts = rank_sums;
+        fa.count = nranks;
+        fa.res = o->d_res;
+        fa.divisor = grad_divisor;
+        fa.max_norm = max_norm;
+        if (any_group_divisor(o)) {
+            fa.gscale = o->d_gscale;
+            fa.ngroups = (int32_t)o->groups.size();
+            fill_divisors(o, grad_divisor, fa.inv_divisor);
+        }
         if ((e = (cudaError_t)soma::launch_finish(fa, stream)) != cudaSuccess)
             return o->cuda_fail(e, "launching the finish kernel");
     } else {
@@ -742,7 +744,9 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         na.res = o->d_res;
         na.divisor = grad_divisor;
         na.max_norm = max_norm;
-        fill_divisors(o, grad_divisor, na.inv_divisor, nullptr);
+        fill_divisors(o, grad_divisor, na.inv_divisor);
+        na.gscale = o->d_gscale;
+        na.ngroups = (int32_t)o->groups.size();
         if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o))) !=
             cudaSuccess)
             return o->cuda_fail(e, "launching the square-sum kernel");
@@ -809,7 +813,9 @@ soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n,
     na.divisor = grad_divisor;
     na.max_norm = 1.0;
     na.sumsq_out = sumsq_out;
-    fill_divisors(o, grad_divisor, na.inv_divisor, nullptr);
+    fill_divisors(o, grad_divisor, na.inv_divisor);
+    na.gscale = o->d_gscale;
+    na.ngroups = (int32_t)o->groups.size();
     cudaError_t e;
     if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o))) != cudaSuccess)
         return o->cuda_fail(e, "launching the square-sum kernel");
@@ -881,17 +887,20 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
     na.dhp = o->d_hp;
     na.present = present;
     na.ngroups = (int32_t)o->groups.size();
-    fill_divisors(o, grad_divisor, na.inv_divisor, nullptr);
+    na.gscale = o->d_gscale;
+    fill_divisors(o, grad_divisor, na.inv_divisor);
     soma::UpdateArgs ua{};
     ua.t = o->upd_tab;
     ua.res = o->d_res;
     ua.dhp = o->d_hp;
     ua.ngroups = (int32_t)o->groups.size();
-    fill_divisors(o, grad_divisor, nullptr, ua.divisor);
-    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, true, any_group_divisor(o))) != cudaSuccess)
+    ua.gscale = o->d_gscale;
+    // one CTA more than the chunks need: CTA 0 derives the group constants
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid + 1, stream, true, any_group_divisor(o))) !=
+        cudaSuccess)
         return o->cuda_fail(e, "launching the square-sum kernel");
     if (o->upd_grid > 0 &&
-        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true, false, any_group_divisor(o))) !=
+        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true, true, any_group_divisor(o))) !=
             cudaSuccess)
         return o->cuda_fail(e, "launching the update kernel");
     o->graph_locked = true;
@@ -1074,6 +1083,7 @@ void soma_opt_destroy(soma_opt_t h) {
             if (pl.d_tables) cudaFree(pl.d_tables);
         if (o->d_groups) cudaFree(o->d_groups);
         if (o->d_hp) cudaFree(o->d_hp);
+        if (o->d_gscale) cudaFree(o->d_gscale);
         if (o->h_res) cudaFreeHost(o->h_res);
         if (o->h_staging) cudaFreeHost(o->h_staging);
         if (o->h_groups) cudaFreeHost(o->h_groups);

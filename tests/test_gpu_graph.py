@@ -2,6 +2,7 @@
 with fresh gradients and a changing learning rate, checked against the fp64
 oracle after every replay; plus the rules that keep a captured graph valid."""
 import math
+from dataclasses import replace
 
 import numpy as np
 import pytest
@@ -81,23 +82,55 @@ def test_captured_step_replays_match_the_oracle(lr_route):
         opt.close()
 
 
-def test_graph_step_equals_regular_step():
-    w = W.with_steps(W.SMALL["action_expert"](), 4)
-    finals = []
+@pytest.mark.parametrize("group_div", [False, True])
+def test_graph_replays_equal_regular_steps_bit_for_bit(group_div):
+    # Regular steps derive each group's constants on the host, graph replays
+    # on the device, with the same fp64 operations rounded one at a time: the
+    # weights and moments agree bit for bit, also after a resume at a large
+    # step count and with a learning rate that changes every step.
+    w = W.with_steps(W.SMALL["hsdp_shard"](), 4)  # two groups, bf16 grads, replicated tensors
+    if group_div:
+        w = replace(w, groups=(replace(w.groups[0], divisor=3.0), w.groups[1]))
+    resume = (123457, 7)
+    finals, norms = [], []
     for graph_mode in (False, True):
         params = W.draw_params(w, "cpu")
         dl = DeviceList(w, params)
         opt = make_opt(w)
-        if graph_mode:
-            opt.push_groups()
+        for q, t in enumerate(resume):
+            opt.set_group_step(q, t)
+        stream = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        got = []
         for s in range(1, w.steps + 1):
             dl.load_grads(W.draw_grads(w, s, "cpu"))
-            (opt.step_graph if graph_mode else opt.step)(dl.tl, w.grad_divisor, w.max_norm)
+            for q in range(len(w.groups)):
+                opt.set_lr(q, w.groups[q].lr * (1.0 + 0.37 * s + 0.11 * q))
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                if not graph_mode:
+                    opt.step(dl.tl, w.grad_divisor, w.max_norm, stream)
+                else:
+                    opt.push_groups(stream)
+                    if s == 1:
+                        opt.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)
+                        with torch.cuda.graph(graph, stream=stream):
+                            opt.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)
+                    else:
+                        graph.replay()
+            got.append(opt.get_norm(stream))
+            torch.cuda.current_stream().wait_stream(stream)
         torch.cuda.synchronize()
-        finals.append([x.cpu().double().numpy() for x in dl.p + dl.m + dl.v])
+        if graph_mode:
+            opt.pull_groups(stream)
+        assert [opt.get_group_step(q) for q in range(len(w.groups))] == [t + w.steps for t in resume]
+        finals.append([x.cpu().view(torch.int32) for x in dl.p + dl.m + dl.v])
+        norms.append(got)
+        del graph
         opt.close()
-    for a, b in zip(*finals):
-        assert_close("graph vs regular", b, a, rtol=1e-6, atol=1e-12)
+    assert norms[0] == norms[1]
+    for k, (a, b) in enumerate(zip(*finals)):
+        assert torch.equal(a, b), k
 
 
 def test_rules_that_keep_a_captured_graph_valid():
