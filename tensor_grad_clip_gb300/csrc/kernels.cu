@@ -100,8 +100,11 @@ __device__ __forceinline__ float block_sum(float x, float* scratch) {
     return r;  // valid in thread 0
 }
 
+// fp64 block sum (valid in thread 0).  An fp64 add takes about 128 cycles
+// on this GPU, so the second level runs only log2(BLOCK / 32) butterfly steps.
 template <int BLOCK>
 __device__ __forceinline__ double block_sum64(double x, double* scratch) {
+    static_assert(BLOCK % 64 == 0 && ((BLOCK / 32) & (BLOCK / 32 - 1)) == 0, "power-of-two warp count");
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -111,9 +114,19 @@ __device__ __forceinline__ double block_sum64(double x, double* scratch) {
     if (w == 0) {
         r = (l < BLOCK / 32) ? scratch[l] : 0.0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        for (int o = BLOCK / 64; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
     }
     return r;
+}
+
+// min(1, max_norm / (norm + 1e-6)), NaN propagating.  The quotient is formed
+// only when it can be below 1: when max_norm >= norm + 1e-6 it rounds to at
+// least 1 anyway, and an fp64 division takes about 550 cycles on this GPU.
+__device__ __forceinline__ double clip_coefficient(double norm, double max_norm) {
+    const double x = norm + 1e-6;
+    if (max_norm >= x) return 1.0;
+    const double q = max_norm / x;  // NaN when norm is NaN
+    return q < 1.0 ? q : (q == q ? 1.0 : q);
 }
 
 // ---- square-sum of one segment, accumulated into a0 / a1 -----------------
@@ -350,22 +363,21 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
         double x[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) x[u] = __ldcg(a.partials + i + u * B);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) s += x[u];
+        // pairwise: three dependent fp64 adds rather than eight
+        s += ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
     }
     for (; i < n; i += B) s += __ldcg(a.partials + i);
     s = block_sum64<kNormBlock>(s, wsum64);
     if (threadIdx.x == 0) {
-        const double norm = kGroupDiv ? sqrt(s) : sqrt(s) / a.divisor;
-        const double q = a.max_norm / (norm + 1e-6);
-        const double coef = (q < 1.0 || q != q) ? q : 1.0;  // NaN propagates
+        const double norm = kGroupDiv ? sqrt(s) : sqrt(s) * a.inv_step_divisor;
+        const double coef = clip_coefficient(norm, a.max_norm);
         a.res->sumsq = s;
         a.res->norm = norm;
         a.res->coef = coef;
-        a.res->scale = (float)(coef / a.divisor);
+        a.res->scale = (float)(coef * a.inv_step_divisor);
         a.res->nonfinite = isfinite(norm) ? 0u : 1u;
         a.res->ticket = 0u;
-        if (a.sumsq_out) *a.sumsq_out = kGroupDiv ? s : s / (a.divisor * a.divisor);
+        if (a.sumsq_out) *a.sumsq_out = kGroupDiv ? s : s * a.inv_step_divisor * a.inv_step_divisor;
         wsum64[0] = coef;
     }
     if (kGroupDiv) {
@@ -383,12 +395,11 @@ __global__ void finish_kernel(const __grid_constant__ FinishArgs a) {
     double s = 0.0;
     for (int r = 0; r < a.count; ++r) s += a.parts[r];
     const double norm = sqrt(s);
-    const double q = a.max_norm / (norm + 1e-6);
-    const double coef = (q < 1.0 || q != q) ? q : 1.0;
+    const double coef = clip_coefficient(norm, a.max_norm);
     a.res->sumsq = s;
     a.res->norm = norm;
     a.res->coef = coef;
-    a.res->scale = (float)(coef / a.divisor);
+    a.res->scale = (float)(coef * a.inv_step_divisor);
     a.res->nonfinite = isfinite(norm) ? 0u : 1u;
     if (a.gscale)
         for (int q = 0; q < a.ngroups && q < kMaxGroups; ++q) a.gscale[q] = (float)(coef * a.inv_divisor[q]);

@@ -186,6 +186,7 @@ extern "C" soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tenso
     a.partials = reinterpret_cast<double*>(d + o_part);
     a.res = reinterpret_cast<soma::Result*>(d);
     a.divisor = grad_divisor;
+    a.inv_step_divisor = 1.0 / grad_divisor;
     a.max_norm = max_norm;
     for (double& w : a.inv_divisor) w = 1.0 / grad_divisor;  // every segment is group 0 here
     if (soma::launch_norm(a, (int)std::max<int64_t>(nchunk, 1), stream) != cudaSuccess) return SOMA_ERR_CUDA;

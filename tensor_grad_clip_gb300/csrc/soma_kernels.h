@@ -141,7 +141,8 @@ struct NormArgs {
     Table t;
     double* partials;       // one per chunk
     Result* res;
-    double divisor;         // the step's divisor (for Result::scale)
+    double divisor;         // the step's divisor d
+    double inv_step_divisor;  // 1 / d, rounded once (fp64 division is slow on the device)
     double max_norm;
     double inv_divisor[kMaxGroups];  // 1 / (effective divisor) of each group
     // group divisors only: the last CTA writes c / d of each group here
@@ -165,6 +166,7 @@ struct FinishArgs {
     int32_t count;
     Result* res;
     double divisor;
+    double inv_step_divisor;
     double max_norm;
     // group divisors only: gscale[q] = c / d_q for q < ngroups
     float* gscale;

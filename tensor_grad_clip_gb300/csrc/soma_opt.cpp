@@ -729,6 +729,7 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         fa.count = nranks;
         fa.res = o->d_res;
         fa.divisor = grad_divisor;
+        fa.inv_step_divisor = 1.0 / grad_divisor;
         fa.max_norm = max_norm;
         if (any_group_divisor(o)) {
             fa.gscale = o->d_gscale;
@@ -743,6 +744,7 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         na.partials = o->d_partials;
         na.res = o->d_res;
         na.divisor = grad_divisor;
+        na.inv_step_divisor = 1.0 / grad_divisor;
         na.max_norm = max_norm;
         fill_divisors(o, grad_divisor, na.inv_divisor);
         na.gscale = o->d_gscale;
@@ -811,6 +813,7 @@ soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n,
     na.partials = o->d_partials;
     na.res = o->d_res;
     na.divisor = grad_divisor;
+    na.inv_step_divisor = 1.0 / grad_divisor;
     na.max_norm = 1.0;
     na.sumsq_out = sumsq_out;
     fill_divisors(o, grad_divisor, na.inv_divisor);
@@ -882,6 +885,7 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
     na.partials = o->d_partials;
     na.res = o->d_res;
     na.divisor = grad_divisor;
+    na.inv_step_divisor = 1.0 / grad_divisor;
     na.max_norm = max_norm;
     na.dgroups = o->d_groups;
     na.dhp = o->d_hp;
