@@ -106,3 +106,57 @@ def test_tuning_drops_prepared_lists():
         if t.trainable:
             assert_close(f"{t.name} p", dl.p[k].cpu().numpy(), orc.params[k])
     opt.close()
+
+
+def test_pipelined_uploads_equal_serial_steps_bit_for_bit():
+    # Gradients arrive from pinned host memory.  Pipelined: two device buffers
+    # used in turn; step t+1's upload runs on a copy stream while step t's
+    # kernels run, each step waits only for its own upload, and an upload
+    # waits for the step that last read its buffer.  Serial: one buffer,
+    # copy then step.  Both must leave the same bits.
+    w = _workload(6)
+    params = W.draw_params(w, "cpu")
+    host = [[g.reshape(-1).pin_memory() for g in W.draw_grads(w, s, "cpu")] for s in range(1, w.steps + 1)]
+    finals = []
+    for pipelined in (False, True):
+        dl = DeviceList(w, params)
+        opt = make_opt(w)
+        main = torch.cuda.current_stream()
+        if not pipelined:
+            for s in range(w.steps):
+                for dst, src in zip(dl.g, host[s]):
+                    dst.copy_(src, non_blocking=True)
+                opt.step(dl.tl, w.grad_divisor, w.max_norm, main)
+        else:
+            gs2 = [torch.empty_like(g) for g in dl.g]
+            tl2 = TensorList(dl.p, gs2, dl.m, dl.v, groups=[t.group for t in w.tensors],
+                             trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
+            bufs = [(dl.g, dl.tl), (gs2, tl2)]
+            cs = torch.cuda.Stream()
+            copied = [torch.cuda.Event(), torch.cuda.Event()]
+            freed = [torch.cuda.Event(), torch.cuda.Event()]
+
+            def upload(s):
+                b = s % 2
+                cs.wait_event(freed[b])
+                with torch.cuda.stream(cs):
+                    for dst, src in zip(bufs[b][0], host[s]):
+                        dst.copy_(src, non_blocking=True)
+                copied[b].record(cs)
+
+            cs.wait_stream(main)
+            upload(0)
+            for s in range(w.steps):
+                b = s % 2
+                main.wait_event(copied[b])
+                opt.step(bufs[b][1], w.grad_divisor, w.max_norm, main)
+                freed[b].record(main)
+                if s + 1 < w.steps:
+                    upload(s + 1)
+            assert opt.cache_stats()["builds"] == 2
+        torch.cuda.synchronize()
+        dl.check_guards()
+        finals.append([x.cpu().view(torch.int32) for x in dl.p + dl.m + dl.v])
+        opt.close()
+    for k, (a, b) in enumerate(zip(*finals)):
+        assert torch.equal(a, b), k
