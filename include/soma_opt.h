@@ -87,7 +87,8 @@ typedef soma_opt *soma_opt_t;
  *               weights, overwritten in the same pass with the updated fp32
  *               weights rounded to nearest even (RLinf's FP32MasterAdamW:
  *               bf16/fp16 parameters with an fp32 master copy); 2-byte aligned.
- *   numel       >= 0.
+ *   numel       >= 0.  An empty entry (0) is never read or written; its
+ *               pointers may be NULL, with or without a copy dtype.
  *   group       id from soma_opt_add_group; ignored when frozen.
  *   grad_dtype  SOMA_DTYPE_F32, _BF16 or _F16; ignored when frozen.
  *   trainable   0 = frozen: never read, never written, not in the norm; its

@@ -171,7 +171,10 @@ soma_status_t validate_entry(soma_opt* o, const soma_tensor_t& t, int64_t k) {
                        o->groups.size());
     if (t.grad_dtype != SOMA_DTYPE_F32 && t.grad_dtype != SOMA_DTYPE_BF16 && t.grad_dtype != SOMA_DTYPE_F16)
         return o->fail(SOMA_ERR_DTYPE, "list[%lld].grad_dtype = %d", (long long)k, (int)t.grad_dtype);
-    if (t.param_lowp ? (t.lowp_dtype != SOMA_DTYPE_BF16 && t.lowp_dtype != SOMA_DTYPE_F16) : t.lowp_dtype != 0)
+    // A copy dtype without a copy is an error, except for an empty tensor, whose
+    // buffers may all be NULL (an empty torch tensor has no storage).
+    if (t.param_lowp ? (t.lowp_dtype != SOMA_DTYPE_BF16 && t.lowp_dtype != SOMA_DTYPE_F16)
+                     : (t.lowp_dtype != 0 && t.numel > 0))
         return o->fail(SOMA_ERR_DTYPE, "list[%lld]: lowp_dtype = %d does not match param_lowp", (long long)k,
                        (int)t.lowp_dtype);
     if (t.numel == 0) return SOMA_OK;

@@ -28,11 +28,15 @@ SENTINEL_F32 = 0x7FC0DEAD     # a NaN payload no computation produces
 SENTINEL_BF16 = 0x7FAD
 
 
-def assert_close(name, got, ref, rtol=RTOL, atol=ATOL):
+def assert_close(name, got, ref, rtol=RTOL, atol=ATOL, tensor_rtol=0.0):
+    """Per element |got - ref| <= rtol |ref| + atol, plus tensor_rtol times
+    the tensor's largest |ref| when given (see run_parity)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
     bound = rtol * np.abs(ref) + atol
+    if tensor_rtol and ref.size:
+        bound = bound + tensor_rtol * float(np.max(np.abs(ref)))
     bad = ~(err <= bound)
     if bad.any():
         i = int(np.argmax(np.where(bad, err / bound, 0)))
@@ -152,10 +156,18 @@ def make_oracle(w: W.Workload, params_cpu) -> OracleOptimizer:
     return OracleOptimizer([p.double().numpy().reshape(-1) for p in params_cpu], flags, groups)
 
 
-def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=None, check_every_step=True):
+def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=None, check_every_step=True,
+               tensor_rtol=0.0):
     """Chained steps of `w` on the GPU and in the oracle, compared after
     every step.  Returns the list of (gpu_norm, oracle_norm, gpu_coef,
-    oracle_coef) per step."""
+    oracle_coef) per step.
+
+    tensor_rtol adds that fraction of each tensor's largest |value| to the
+    per-element bound.  fp32 evaluation of m = beta1 m + (1 - beta1) g' errs
+    by about 2^-24 of its two terms, not of their difference: where they
+    cancel, the element-relative bound cannot hold whatever the kernel does.
+    The workloads' gradients keep the terms small enough that it does; lists
+    with large gradients need this term."""
     steps = w.steps if steps is None else steps
     params = W.draw_params(w, "cpu")
     dl = DeviceList(w, params, shift=shift, frozen_null=frozen_null)
@@ -188,9 +200,9 @@ def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=
             for k, t in enumerate(w.tensors):
                 if not t.trainable:
                     continue
-                assert_close(f"step {s} {t.name} p", dl.p[k].cpu().numpy(), orc.params[k])
-                assert_close(f"step {s} {t.name} m", dl.m[k].cpu().numpy(), orc.exp_avg[k])
-                assert_close(f"step {s} {t.name} v", dl.v[k].cpu().numpy(), orc.exp_avg_sq[k])
+                assert_close(f"step {s} {t.name} p", dl.p[k].cpu().numpy(), orc.params[k], tensor_rtol=tensor_rtol)
+                assert_close(f"step {s} {t.name} m", dl.m[k].cpu().numpy(), orc.exp_avg[k], tensor_rtol=tensor_rtol)
+                assert_close(f"step {s} {t.name} v", dl.v[k].cpu().numpy(), orc.exp_avg_sq[k], tensor_rtol=tensor_rtol)
         for q in range(len(w.groups)):
             assert opt.get_group_step(q) == orc.groups[q].step
     opt.close()

@@ -154,6 +154,21 @@ def test_step_rejects_null_list_and_negative_count():
     opt.close()
 
 
+def test_empty_entry_may_have_null_buffers_and_a_copy_dtype():
+    # an empty torch tensor has no storage: data_ptr() is 0 for every buffer
+    opt = SomaOpt(0)
+    opt.add_group(lr=1e-3)
+    empty = _entry(param=0, grad=0, exp_avg=0, exp_avg_sq=0, numel=0, lowp_dtype=1)
+    bad = _entry(grad_dtype=9)
+    # the empty entry passes validation; the second entry is what fails
+    assert _step(opt, [empty, bad]) == _abi.SOMA_ERR_DTYPE
+    assert b"list[1]" in _abi.soma_opt_last_error(opt.handle)
+    # a copy dtype without a copy stays an error for a non-empty entry
+    assert _step(opt, [_entry(lowp_dtype=1), bad]) == _abi.SOMA_ERR_DTYPE
+    assert b"list[0]" in _abi.soma_opt_last_error(opt.handle)
+    opt.close()
+
+
 def test_frozen_entries_may_have_null_buffers_and_any_group():
     opt = SomaOpt(0)
     opt.add_group(lr=1e-3)
