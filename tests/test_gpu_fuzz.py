@@ -56,3 +56,49 @@ def _random_case(seed):
 def test_random_list(seed):
     w, shifts, tuning = _random_case(seed)
     run_parity(w, shift=shifts, tuning=tuning, tensor_rtol=1e-6)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_list_graph_replays_equal_regular_steps(seed):
+    # The graph step derives each group's constants on the device; on the
+    # random lists (beta1 = 0, group divisors, model copies, resumed step
+    # counts) its replays must leave the same bits as regular steps.
+    import torch
+    from parity_harness import DeviceList, make_opt
+    w, shifts, tuning = _random_case(seed)
+    w = W.with_steps(w, 3)
+    finals = []
+    for graph_mode in (False, True):
+        dl = DeviceList(w, W.draw_params(w, "cpu"), shift=shifts)
+        opt = make_opt(w)
+        if tuning:
+            opt.set_tuning(**tuning)
+        for q in range(len(w.groups)):
+            opt.set_group_step(q, 1000 * q)
+        stream = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        norms = []
+        for s in range(1, w.steps + 1):
+            dl.load_grads(W.draw_grads(w, s, "cpu"))
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                if not graph_mode:
+                    opt.step(dl.tl, w.grad_divisor, w.max_norm, stream)
+                else:
+                    opt.push_groups(stream)
+                    if s == 1:
+                        opt.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)
+                        with torch.cuda.graph(graph, stream=stream):
+                            opt.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)
+                    else:
+                        graph.replay()
+            norms.append(opt.get_norm(stream))
+            torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        dl.check_guards()
+        finals.append((norms, [x.cpu().view(torch.int32) for x in dl.p + dl.m + dl.v]))
+        del graph
+        opt.close()
+    assert finals[0][0] == finals[1][0]
+    for k, (a, b) in enumerate(zip(finals[0][1], finals[1][1])):
+        assert torch.equal(a, b), k
