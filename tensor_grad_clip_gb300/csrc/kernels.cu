@@ -129,6 +129,17 @@ __device__ __forceinline__ double clip_coefficient(double norm, double max_norm)
     return q < 1.0 ? q : (q == q ? 1.0 : q);
 }
 
+// Read-only 16-byte load of gradient words that this kernel reads once: not
+// allocated in L1 (same-box A/B: the square-sum kernel 7 % faster on the
+// action-expert list, 10 % on the 20 000-tensor list).
+__device__ __forceinline__ uint4 ld_once(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // ---- square-sum of one segment, accumulated into a0 / a1 -----------------
 
 template <int DT>
@@ -199,8 +210,8 @@ __device__ __forceinline__ void segment_sumsq(const Seg& s, float& a0, float& a1
     const int U = DT == kF32 ? 2 * s.nvec : s.nvec;
     int u = threadIdx.x;
     for (; u + 3 * B < U; u += 4 * B) {
-        const uint4 w0 = __ldg(base + u), w1 = __ldg(base + u + B);
-        const uint4 w2 = __ldg(base + u + 2 * B), w3 = __ldg(base + u + 3 * B);
+        const uint4 w0 = ld_once(base + u), w1 = ld_once(base + u + B);
+        const uint4 w2 = ld_once(base + u + 2 * B), w3 = ld_once(base + u + 3 * B);
         if (DT == kF32) {
             sq4_f32(make_float4(__uint_as_float(w0.x), __uint_as_float(w0.y), __uint_as_float(w0.z),
                                 __uint_as_float(w0.w)), a0, a1);
@@ -218,7 +229,7 @@ __device__ __forceinline__ void segment_sumsq(const Seg& s, float& a0, float& a1
         }
     }
     for (; u < U; u += B) {
-        const uint4 w = __ldg(base + u);
+        const uint4 w = ld_once(base + u);
         if (DT == kF32)
             sq4_f32(make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
                                 __uint_as_float(w.w)), a0, a1);
@@ -256,7 +267,7 @@ __device__ __forceinline__ void chunk_sumsq(const Seg* segs, const int* upre, co
                 const Seg& sg = segs[k];
                 dt[q] = sg.gdtype;
                 const char* base = static_cast<const char*>(sg.g) + sg.head * (sg.gdtype == kF32 ? 4 : 2);
-                w[q] = __ldg(reinterpret_cast<const uint4*>(base) + (u - upre[k]));
+                w[q] = ld_once(reinterpret_cast<const uint4*>(base) + (u - upre[k]));
             }
         }
 #pragma unroll
