@@ -187,12 +187,20 @@ soma_status_t validate_entry(soma_opt* o, const soma_tensor_t& t, int64_t k) {
     return SOMA_OK;
 }
 
-// Smallest h in [0, 8) at which every listed buffer is 16-byte aligned, or -1.
+// Head h in [0, 8) of a tensor's vector body: the smallest at which every
+// fp32 buffer is 32-byte aligned and every 16-bit one 16-byte aligned (the
+// update kernel then moves eight fp32 values per access), else the smallest
+// at which every buffer is 16-byte aligned, else -1 (one element at a time).
 int vector_head(const uintptr_t* addr, const int* esize, int n) {
-    for (int h = 0; h < soma::kVec; ++h) {
-        bool ok = true;
-        for (int k = 0; k < n && ok; ++k) ok = (addr[k] + (uintptr_t)h * esize[k]) % 16 == 0;
-        if (ok) return h;
+    for (int wide = 1; wide >= 0; --wide) {
+        for (int h = 0; h < soma::kVec; ++h) {
+            bool ok = true;
+            for (int k = 0; k < n && ok; ++k) {
+                const uintptr_t a = (wide && esize[k] == 4) ? 32 : 16;
+                ok = (addr[k] + (uintptr_t)h * esize[k]) % a == 0;
+            }
+            if (ok) return h;
+        }
     }
     return -1;
 }
