@@ -1,7 +1,8 @@
 """Parity at full size, in the layout and launch configuration bench.py times.
 
-For the action-expert (302 M), 7B shard-view (6.48 G) and flat (1.5 G)
-lists, over 10 chained steps:
+The 20 000-tensor list (104 M) is compared element by element after each of
+3 chained steps.  For the action-expert (302 M), 7B shard-view (6.48 G) and
+flat (1.5 G) lists, over 10 chained steps:
 
 * the norm is the oracle's own fp64 sum over every owned gradient, taken
   in pieces of at most 2^26 elements on a thread pool and added in list
@@ -134,3 +135,45 @@ def test_tensor_beyond_2_pow_31_elements():
                    steps=2, grad_std=1e-3, seed=77)
     around = np.arange((1 << 31) - 20, (1 << 31) + 13)
     run_full(w, steps=2, extra_idx=around)
+
+
+def test_full_size_many_small_every_element():
+    # The 20 000-tensor list at full size (104 M trainable elements), every
+    # element against the oracle after each of 3 chained steps.  The flat
+    # buffers come back to the host once per step and are sliced per tensor.
+    from parity_harness import make_oracle
+    w = W.with_steps(W.FULL["many_small"](), 3)
+    dev = torch.device("cuda", 0)
+    fb = W.FlatBuffers(w, dev, grad_step=1)
+    P0 = fb.P.cpu()
+    sl = [slice(fb.offsets[k], fb.offsets[k] + t.numel) for k, t in enumerate(w.tensors)]
+    orc = make_oracle(w, [P0[s_] for s_ in sl])
+    opt = SomaOpt(0)
+    for q in w.groups:
+        opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+    tl = TensorList(fb.p, fb.g, fb.m, fb.v, groups=[t.group for t in w.tensors],
+                    trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
+    for s in range(1, w.steps + 1):
+        if s > 1:
+            fb.load_grads(s)
+        G = fb.G.cpu()
+        opt.step(tl, w.grad_divisor, w.max_norm)
+        norm, coef, nonfinite = opt.get_norm()
+        rn, rc = orc.step([G[s_] for s_ in sl], w.grad_divisor, w.max_norm)
+        assert not nonfinite
+        assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (s, norm, rn)
+        assert math.isclose(coef, rc, rel_tol=NORM_RTOL), (s, coef, rc)
+        assert torch.equal(fb.G.cpu().view(torch.int32), G.view(torch.int32)), "gradients changed"
+        P, M, V = fb.P.cpu().numpy(), fb.M.cpu().numpy(), fb.V.cpu().numpy()
+        for k, t in enumerate(w.tensors):
+            if t.trainable:
+                assert_close(f"step {s} {t.name} p", P[sl[k]], orc.params[k])
+                assert_close(f"step {s} {t.name} m", M[sl[k]], orc.exp_avg[k])
+                assert_close(f"step {s} {t.name} v", V[sl[k]], orc.exp_avg_sq[k])
+            elif t.numel:
+                assert np.array_equal(P[sl[k]].view(np.int32), P0[sl[k]].numpy().view(np.int32))
+    torch.cuda.synchronize()
+    assert fb.gaps_intact(), "a write landed outside a tensor"
+    opt.close()
+    del fb
+    torch.cuda.empty_cache()
