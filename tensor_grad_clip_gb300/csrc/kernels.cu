@@ -326,6 +326,15 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
     // has started; it waits for this grid's results before using them.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    const int first = kGraph ? (int)blockIdx.x - 1 : (int)blockIdx.x;
+    const int stride = kGraph ? (int)gridDim.x - 1 : (int)gridDim.x;
+    // This kernel itself may start before the preceding kernel on the stream
+    // has finished (programmatic serialization): stage the first chunk's
+    // segments (the tables only), then wait for that kernel before reading
+    // any gradient or writing anything another kernel reads.
+    const int ns0 = (first >= 0 && first < a.t.nchunks) ? stage_segments(a.t, first, segs) : 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // Graph steps: CTA 0 advances the step counts and derives the group
     // constants (they do not depend on the norm), alongside the chunk CTAs
     // rather than after the reduction.
@@ -338,10 +347,8 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
             }
         }
     }
-    const int first = kGraph ? (int)blockIdx.x - 1 : (int)blockIdx.x;
-    const int stride = kGraph ? (int)gridDim.x - 1 : (int)gridDim.x;
     for (int c = first; c >= 0 && c < a.t.nchunks; c += stride) {
-        const int ns = stage_segments(a.t, c, segs);
+        const int ns = c == first ? ns0 : stage_segments(a.t, c, segs);
         float a0 = 0.f, a1 = 0.f;
         if (ns == 1) {
             if (segs[0].gdtype == kBF16) segment_sumsq<kBF16>(segs[0], a0, a1);
@@ -731,6 +738,9 @@ __device__ __forceinline__ void chunk_update(const Seg* segs, const int* vpre, c
 // group; otherwise every element uses the one scale the norm kernel wrote.
 template <bool kGraph, bool kGroupDiv>
 __global__ void __launch_bounds__(kUpdateBlock, 2) update_kernel(const __grid_constant__ UpdateArgs a) {
+    // The next step's square-sum kernel may be scheduled once every CTA of
+    // this one has started; it waits for this grid before reading gradients.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];
     __shared__ int vpre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
     __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
@@ -784,12 +794,23 @@ __global__ void __launch_bounds__(kUpdateBlock, 2) update_kernel(const __grid_co
 
 }  // namespace
 
-int launch_norm(const NormArgs& a, int grid, void* stream, bool graph, bool group_div) {
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (graph && group_div) norm_kernel<true, true><<<grid, kNormBlock, 0, s>>>(a);
-    else if (graph) norm_kernel<true, false><<<grid, kNormBlock, 0, s>>>(a);
-    else if (group_div) norm_kernel<false, true><<<grid, kNormBlock, 0, s>>>(a);
-    else norm_kernel<false, false><<<grid, kNormBlock, 0, s>>>(a);
+int launch_norm(const NormArgs& a, int grid, void* stream, bool graph, bool group_div, bool overlap) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kNormBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    cudaError_t e;
+    if (graph && group_div) e = cudaLaunchKernelEx(&cfg, norm_kernel<true, true>, a);
+    else if (graph) e = cudaLaunchKernelEx(&cfg, norm_kernel<true, false>, a);
+    else if (group_div) e = cudaLaunchKernelEx(&cfg, norm_kernel<false, true>, a);
+    else e = cudaLaunchKernelEx(&cfg, norm_kernel<false, false>, a);
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 

@@ -190,10 +190,13 @@ constexpr int kUpdateBlock = 256;
 // graph = true selects the variants that take group constants from device
 // memory (NormArgs::dgroups / dhp, UpdateArgs::dhp).
 // group_div: some group of the list sets its own divisor (NormArgs::inv_divisor).
-int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false, bool group_div = false);
-// overlap = true launches with programmatic stream serialization: the update
-// kernel may start while the previous kernel on the stream finishes, and waits
-// (griddepcontrol.wait) before it reads that kernel's results.
+// overlap (here and for launch_update) = true launches with programmatic
+// stream serialization: the kernel may start while the previous kernel on the
+// stream finishes, and waits (griddepcontrol.wait) before it reads anything
+// that kernel may write.  The update kernel lets the next square-sum kernel
+// start this way, and the square-sum kernel the update kernel.
+int launch_norm(const NormArgs& a, int grid, void* stream, bool graph = false, bool group_div = false,
+                bool overlap = false);
 int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = false, bool overlap = false,
                   bool group_div = false);
 int launch_finish(const FinishArgs& a, void* stream);

@@ -760,7 +760,8 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         fill_divisors(o, grad_divisor, na.inv_divisor);
         na.gscale = o->d_gscale;
         na.ngroups = (int32_t)o->groups.size();
-        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o))) !=
+        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o),
+                                                ev == nullptr)) !=
             cudaSuccess)
             return o->cuda_fail(e, "launching the square-sum kernel");
     }
@@ -831,7 +832,8 @@ soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n,
     na.gscale = o->d_gscale;
     na.ngroups = (int32_t)o->groups.size();
     cudaError_t e;
-    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o))) != cudaSuccess)
+    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o), true)) !=
+        cudaSuccess)
         return o->cuda_fail(e, "launching the square-sum kernel");
     if ((e = cudaEventRecord(o->done, (cudaStream_t)stream)) != cudaSuccess)
         return o->cuda_fail(e, "cudaEventRecord");
