@@ -556,8 +556,12 @@ def run_ours(args):
                 "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth",
                 "traffic": ncu_traffic(w.name), "algorithmic_bytes_per_launch": upd_bytes,
                 "avg_launch_ms": upd_avg_ms,
-                "norm_kernel": {"achieved": norm_bytes / (norm_avg_ms / 1e3) / 1e9 if norm_avg_ms > 0 else None,
+                "norm_kernel": {"achieved": norm_bytes / (norm_avg_ms / 1e3) / 1e9
+                                if norm_avg_ms > 0 and world == 1 else None,
                                 "avg_launch_ms": norm_avg_ms, "algorithmic_bytes_per_launch": norm_bytes}}
+    if world > 1:
+        roofline["norm_kernel"]["note"] = ("several ranks: the square-sum runs in soma_opt_sumsq before the "
+                                           "all-gather; the events time the finish kernel")
 
     e2e = None
     if not args.no_e2e and graph is None:
@@ -585,7 +589,8 @@ def run_ours(args):
             "effective_hbm_frac_of_8tbs": eff_gbs / 8000.0,
             "algorithmic_hbm_gbs": alg_gbs * world,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": plan["launches_per_step"] * args.steps,
+            # multi-rank steps add the finish kernel (rank-ordered sum of the ranks' square-sums)
+            "gpu_launches": (plan["launches_per_step"] + (1 if world > 1 else 0)) * args.steps,
             "clocks": clocks,
             "last_norm": norm, "last_clip_coef": coef, "nonfinite": nonfinite,
         }
