@@ -7,7 +7,7 @@
 //                   to arrive (atomic ticket; nobody waits) adds the partials
 //                   in fp64 in a fixed order, so the norm is the same bits
 //                   on every run whatever the CTA schedule, then derives
-//                   norm = sqrt(S)/d and c = min(1, max_norm/(norm + 1e-6)).
+//                   norm = sqrt(S) * (1/d) and c = min(1, max_norm/(norm + 1e-6)).
 //                   This is the "statistics needed for one global clipping
 //                   decision" of the SomaSpeed optimizer paragraphs, with
 //                   ownership resolved by the host (only owned segments are
@@ -19,8 +19,12 @@
 //                   g (2 or 4 B) and p, m, v (4 B each) in, p, m, v out.
 //                   Gradients are never written.
 //
-// Both kernels are HBM-bound streams (about 0.5 flop per byte); they use
-// 16-byte vector accesses and no tensor cores.
+// Both kernels are HBM-bound streams (about 0.5 flop per byte); they use 16-
+// and 32-byte vector accesses and no tensor cores.  Consecutive kernels of a
+// step, and of consecutive steps, overlap by programmatic dependent launch:
+// each kernel signals griddepcontrol.launch_dependents at its start, and the
+// next one runs griddepcontrol.wait before it touches anything the previous
+// one may write.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

@@ -14,10 +14,12 @@
 //     SomaSpeed optimizer paragraphs).
 //
 // Vector body: inside a segment, elements [head, head + 8*nvec) are processed
-// eight at a time with 16-byte accesses; the host picks `head` so that every
-// buffer is 16-byte aligned there, and cuts tensors only at such points.  The
-// few elements before and after run one at a time.  A tensor whose buffers
-// cannot all be aligned at one element is processed one element at a time.
+// eight at a time with 16-byte accesses, or 32-byte ones for fp32 buffers
+// that are 32-byte aligned there; the host picks `head` so that every buffer
+// is 16-byte aligned there (32-byte for fp32 ones when possible), and cuts
+// tensors only at such points.  The few elements before and after run one at
+// a time.  A tensor whose buffers cannot all be aligned at one element is
+// processed one element at a time.
 #pragma once
 
 #include <cmath>
