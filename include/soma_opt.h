@@ -150,7 +150,9 @@ soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
  * the device) and the fused update.  No device-to-host synchronisation
  * happens, except that a list the handle has not prepared yet waits for the
  * previous step's kernels before its device tables are written (see the
- * prepared-list cache below). */
+ * prepared-list cache below).  The group constants are fixed when the step is
+ * enqueued, so a capturing `stream` gets SOMA_ERR_STATE: capture
+ * soma_opt_step_graph instead. */
 soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
                             double grad_divisor, double max_norm, void *stream);
 
@@ -216,7 +218,8 @@ soma_status_t soma_opt_device_groups(soma_opt_t opt, soma_device_group_t **table
  *      soma_opt_step; soma_opt_get_norm reports the global norm.
  *
  * Both calls are asynchronous on `stream`; a replicated tensor must be owned
- * by exactly one rank of the group. */
+ * by exactly one rank of the group.  Like soma_opt_step, both return
+ * SOMA_ERR_STATE on a capturing stream. */
 #define SOMA_MAX_RANKS 65536
 soma_status_t soma_opt_sumsq(soma_opt_t opt, const soma_tensor_t *list, int64_t n, double grad_divisor,
                              double *sumsq_out, void *stream);

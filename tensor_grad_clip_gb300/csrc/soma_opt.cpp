@@ -473,6 +473,20 @@ soma_status_t capturing(soma_opt* o, void* stream, bool* yes) {
     return SOMA_OK;
 }
 
+// The regular and multi-rank steps fix their constants (lr, step counts,
+// bias corrections) on the host when they enqueue, and may wait on the host
+// for a new list's tables: a captured launch would replay stale constants, so
+// they refuse stream capture (soma_opt_step_graph is the capturable step).
+soma_status_t refuse_capture(soma_opt* o, void* stream, const char* what) {
+    bool cap = false;
+    soma_status_t st = capturing(o, stream, &cap);
+    if (st != SOMA_OK) return st;
+    if (cap)
+        return o->fail(SOMA_ERR_STATE, "%s cannot be captured in a CUDA graph (its constants are fixed when it is "
+                                       "enqueued); capture soma_opt_step_graph instead", what);
+    return SOMA_OK;
+}
+
 // Common argument checks of the step entry points.  *hit: the prepared list
 // equal to `list`, or -1; only a list not prepared yet is validated entry by
 // entry (a prepared one was validated when it was built, and groups are never
@@ -802,6 +816,7 @@ soma_status_t soma_opt_step(soma_opt_t h, const soma_tensor_t* list, int64_t n, 
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    if ((st = refuse_capture(o, stream, "soma_opt_step")) != SOMA_OK) return st;
     if ((st = prepare(o, list, n, hit, stream)) != SOMA_OK) return st;
     return launch_step(o, grad_divisor, max_norm, nullptr, 0, stream);
 }
@@ -819,6 +834,7 @@ soma_status_t soma_opt_sumsq(soma_opt_t h, const soma_tensor_t* list, int64_t n,
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    if ((st = refuse_capture(o, stream, "soma_opt_sumsq")) != SOMA_OK) return st;
     if ((st = prepare(o, list, n, hit, stream)) != SOMA_OK) return st;
     soma::NormArgs na{};
     na.t = o->norm_tab;
@@ -858,6 +874,7 @@ soma_status_t soma_opt_step_from_sumsq(soma_opt_t h, const soma_tensor_t* list, 
         return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: it keeps that list");
     DeviceGuard dg(o->device);
     if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "selecting the device");
+    if ((st = refuse_capture(o, stream, "soma_opt_step_from_sumsq")) != SOMA_OK) return st;
     if ((st = prepare(o, list, n, hit, stream)) != SOMA_OK) return st;
     return launch_step(o, grad_divisor, max_norm, rank_sumsq, nranks, stream);
 }

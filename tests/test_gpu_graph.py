@@ -161,3 +161,38 @@ def test_rules_that_keep_a_captured_graph_valid():
     opt.step(dl.tl, w.grad_divisor, w.max_norm)  # the same list still works on the regular path
     torch.cuda.synchronize()
     opt.close()
+
+
+def test_regular_and_multirank_steps_refuse_stream_capture():
+    # Their constants are fixed at enqueue time, so a captured launch would
+    # replay stale step counts: capture is refused, and nothing changes.
+    w = W.with_steps(W.SMALL["tiny"](), 2)
+    params = W.draw_params(w, "cpu")
+    dl = DeviceList(w, params)
+    opt = make_opt(w)
+    dl.load_grads(W.draw_grads(w, 1, "cpu"))
+    opt.step(dl.tl, w.grad_divisor, w.max_norm)  # the list is prepared
+    torch.cuda.synchronize()
+    p_before = [x.clone() for x in dl.p]
+    sums = torch.zeros(1, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    calls = (lambda s: opt.step(dl.tl, w.grad_divisor, w.max_norm, s),
+             lambda s: opt.sumsq(dl.tl, w.grad_divisor, sums, s),
+             lambda s: opt.step_from_sumsq(dl.tl, w.grad_divisor, w.max_norm, sums, s))
+    for call in calls:
+        graph = torch.cuda.CUDAGraph()
+        with pytest.raises(SomaError) as e:
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(graph, stream=stream):
+                    call(stream)
+        assert e.value.status == _abi.SOMA_ERR_STATE
+        assert "soma_opt_step_graph" in str(e.value)
+        del graph
+    torch.cuda.synchronize()
+    assert opt.get_group_step(0) == 1
+    for a, b in zip(p_before, dl.p):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    opt.step(dl.tl, w.grad_divisor, w.max_norm)  # still usable outside capture
+    assert opt.get_group_step(0) == 2
+    opt.close()
