@@ -45,14 +45,17 @@ PROFILE_JSON = os.path.join(ROOT, "profiles", "update_kernel_action_expert.json"
 
 def parse_args():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="action_expert")
-    ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1, help="GPUs (one rank each under torchrun)")
+    ap.add_argument("--steps", type=int, default=1000, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=20, help="untimed steps first")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="reference: the fp64 CPU oracle on bounded samples of the same list")
+    ap.add_argument("--workload", default="action_expert",
+                    help="tiny, action_expert, many_small, hsdp_shard or flat")
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="steps per end-to-end window (gradients uploaded from pinned host memory)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end runs")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--tuning", default="",
                     help="update_chunk,norm_chunk,update_ctas_per_sm,norm_ctas_per_sm (0 = default)")
     ap.add_argument("--graph", action="store_true",
