@@ -321,3 +321,35 @@ def test_degenerate_hyperparameters():
         assert torch.equal(before[k].view(torch.int32), dl.p[k].view(torch.int32))
         assert dl.m[k].abs().max().item() > 0
     opt.close()
+
+
+def test_two_handles_on_two_streams_concurrently():
+    # Handles share no state: two lists stepped at the same time on unordered
+    # streams each match their own oracle.
+    wa = W.with_steps(W.SMALL["action_expert"](), 3)
+    wb = W.with_steps(W.SMALL["many_small"](), 3)
+    runs = []
+    for w in (wa, wb):
+        params = W.draw_params(w, "cpu")
+        runs.append((w, DeviceList(w, params), make_opt(w), make_oracle(w, params), torch.cuda.Stream()))
+    for s in range(1, 4):
+        grads = []
+        for w, dl, opt, orc, st in runs:
+            g = W.draw_grads(w, s, "cpu")
+            dl.load_grads(g)
+            grads.append(g)
+        torch.cuda.synchronize()
+        for w, dl, opt, orc, st in runs:  # both enqueued before either is waited on
+            opt.step(dl.tl, w.grad_divisor, w.max_norm, st)
+        for (w, dl, opt, orc, st), g in zip(runs, grads):
+            norm, coef, _ = opt.get_norm(st)
+            rn, rc = orc.step(g, w.grad_divisor, w.max_norm)
+            assert math.isclose(norm, rn, rel_tol=NORM_RTOL) and math.isclose(coef, rc, rel_tol=NORM_RTOL)
+    torch.cuda.synchronize()
+    for w, dl, opt, orc, st in runs:
+        for k, t in enumerate(w.tensors):
+            if t.trainable:
+                assert_close(f"{w.name} {t.name} p", dl.p[k].cpu().numpy(), orc.params[k])
+                assert_close(f"{w.name} {t.name} v", dl.v[k].cpu().numpy(), orc.exp_avg_sq[k])
+        dl.check_guards()
+        opt.close()
