@@ -1,0 +1,25 @@
+"""The boundary is a C ABI: a plain C99 program (tests/c_abi/abi_check.c)
+includes include/soma_opt.h, links the library and drives its host-side
+calls without Python or CUDA work."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+from tensor_grad_clip_gb300 import build
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_c99_program_uses_the_library(tmp_path):
+    lib = build.build()
+    exe = tmp_path / "abi_check"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(HERE, "c_abi", "abi_check.c"), "-o", str(exe), lib,
+                    "-Wl,-rpath," + os.path.dirname(lib)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "c abi ok" in out.stdout
