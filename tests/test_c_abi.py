@@ -23,3 +23,19 @@ def test_c99_program_uses_the_library(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
     assert "c abi ok" in out.stdout
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_c99_program_runs_a_step(tmp_path):
+    # No Python on the path: CUDA runtime buffers, one step, the closed form.
+    lib = build.build()
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = tmp_path / "step_check"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(cuda, "include"), os.path.join(HERE, "c_abi", "step_check.c"),
+                    "-o", str(exe), lib, "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm",
+                    "-Wl,-rpath," + os.path.dirname(lib) + ":" + os.path.join(cuda, "lib64")], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "c step ok" in out.stdout
