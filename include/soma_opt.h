@@ -227,9 +227,12 @@ soma_status_t soma_opt_step_from_sumsq(soma_opt_t opt, const soma_tensor_t *list
                                        double grad_divisor, double max_norm,
                                        const double *rank_sumsq, int32_t nranks, void *stream);
 
-/* Norm and clip coefficient of the last step (fp64), and 1 if that norm was
- * not finite.  Any output pointer may be NULL.  Waits for the last step on
- * `stream`: the only call besides soma_opt_read_timing that blocks. */
+/* Norm and clip coefficient of the last step (fp64), and the number of steps
+ * since the previous soma_opt_get_norm on this handle whose norm was not
+ * finite (so at least 1 if the last step's was not; a loop that reads the norm
+ * only every few steps still learns of a non-finite one in between).  Any
+ * output pointer may be NULL.  Waits for the last step on `stream`: the only
+ * call besides soma_opt_read_timing that blocks. */
 soma_status_t soma_opt_get_norm(soma_opt_t opt, double *norm, double *clip_coef,
                                 int32_t *nonfinite, void *stream);
 

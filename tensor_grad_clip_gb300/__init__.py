@@ -228,7 +228,8 @@ class SomaOpt:
         return p.value
 
     def get_norm(self, stream=None):
-        """(norm, clip_coef, nonfinite) of the last step; waits for it."""
+        """(norm, clip_coef, nonfinite) of the last step; waits for it.
+        nonfinite: steps since the previous call whose norm was not finite."""
         n, c, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_int32()
         self._check(_abi.soma_opt_get_norm(self._h, ctypes.byref(n), ctypes.byref(c), ctypes.byref(f),
                                            _stream_handle(stream)))

@@ -406,6 +406,8 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
         a.res->coef = coef;
         a.res->scale = (float)(coef * a.inv_step_divisor);
         a.res->nonfinite = isfinite(norm) ? 0u : 1u;
+        // (a multi-rank step counts its global norm in the finish kernel)
+        if (!isfinite(norm) && !a.sumsq_out) a.res->nonfinite_steps += 1u;
         a.res->ticket = 0u;
         if (a.sumsq_out) *a.sumsq_out = kGroupDiv ? s : s * a.inv_step_divisor * a.inv_step_divisor;
         wsum64[0] = coef;
@@ -431,6 +433,7 @@ __global__ void finish_kernel(const __grid_constant__ FinishArgs a) {
     a.res->coef = coef;
     a.res->scale = (float)(coef * a.inv_step_divisor);
     a.res->nonfinite = isfinite(norm) ? 0u : 1u;
+    if (!isfinite(norm)) a.res->nonfinite_steps += 1u;
     if (a.gscale)
         for (int q = 0; q < a.ngroups && q < kMaxGroups; ++q) a.gscale[q] = (float)(coef * a.inv_divisor[q]);
 }

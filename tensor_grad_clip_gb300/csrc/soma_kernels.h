@@ -120,7 +120,8 @@ struct Result {
     float scale;            // coef / d in fp32: the update multiplies g by this
     uint32_t nonfinite;     // 1 when norm is not finite
     uint32_t ticket;        // CTA arrival counter; the last CTA resets it to 0
-    uint32_t pad[3];
+    uint32_t nonfinite_steps;  // steps with a non-finite norm since the host last cleared it
+    uint32_t pad[2];
 };
 static_assert(sizeof(Result) == 48, "Result layout");
 

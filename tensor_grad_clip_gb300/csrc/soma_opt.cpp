@@ -86,6 +86,7 @@ struct soma_opt {
     size_t staging_cap = 0;
     cudaEvent_t done = nullptr;     // recorded after each step's last kernel
     bool have_done = false;
+    uint32_t nonfinite_read = 0;    // Result::nonfinite_steps at the last soma_opt_get_norm
     void* last_stream = nullptr;
     soma::DevGroup* d_groups = nullptr;  // graph-capturable step: group table
     soma::GroupHp* d_hp = nullptr;       // and the constants of the current step
@@ -1047,7 +1048,10 @@ soma_status_t soma_opt_get_norm(soma_opt_t h, double* norm, double* clip_coef, i
         return o->cuda_fail(e, "cudaStreamSynchronize");
     if (norm) *norm = o->h_res->norm;
     if (clip_coef) *clip_coef = o->h_res->coef;
-    if (nonfinite) *nonfinite = (int32_t)o->h_res->nonfinite;
+    // the device count only grows; report the steps since the previous read
+    const uint32_t seen = o->h_res->nonfinite_steps;
+    if (nonfinite) *nonfinite = (int32_t)std::min<uint32_t>(seen - o->nonfinite_read, INT32_MAX);
+    o->nonfinite_read = seen;
     return SOMA_OK;
 }
 

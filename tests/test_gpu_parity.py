@@ -150,6 +150,28 @@ def test_nonfinite_gradient(bad):
     opt.close()
 
 
+def test_nonfinite_steps_are_counted_until_read():
+    # A loop that reads the norm only now and then still learns of a step
+    # whose norm was not finite: get_norm counts such steps since its last call.
+    T = W.TensorSpec
+    w = _custom([T("a", (1000,)), T("b", (64,), W.BF16)], steps=4)
+    dl = DeviceList(w, W.draw_params(w, "cpu"))
+    opt = make_opt(w)
+    for s, bad in ((1, False), (2, True), (3, False), (4, True)):
+        grads = W.draw_grads(w, s, "cpu")
+        if bad:
+            grads[0][5] = float("nan")
+        dl.load_grads(grads)
+        opt.step(dl.tl, w.grad_divisor, w.max_norm)
+        if s == 3:
+            norm, coef, nonfinite = opt.get_norm()
+            assert math.isfinite(norm) and nonfinite == 1  # step 2, not the last one
+    norm, coef, nonfinite = opt.get_norm()
+    assert math.isnan(norm) and nonfinite == 1  # step 4 only
+    assert opt.get_norm()[2] == 0               # nothing new since
+    opt.close()
+
+
 def test_golden_example_on_gpu():
     g = golden_fixture.load()
     params = [torch.tensor(t["p0"], dtype=torch.float32) for t in g.tensors]
