@@ -144,6 +144,7 @@ class SomaOpt:
             raise SomaError(st, _abi.soma_opt_last_error(None).decode())
         self._h = h
         self.device = int(device)
+        self._ngroups = 0
 
     def _check(self, st: int):
         if st != 0:
@@ -157,7 +158,39 @@ class SomaOpt:
         gid = ctypes.c_int32()
         self._check(_abi.soma_opt_add_group(self._h, lr, betas[0], betas[1], eps, weight_decay,
                                             ctypes.byref(gid)))
+        self._ngroups = gid.value + 1
         return gid.value
+
+    @property
+    def num_groups(self) -> int:
+        return self._ngroups
+
+    def state_dict(self) -> dict:
+        """What the library holds for a checkpoint: each group's
+        hyperparameters, own divisor and step count (weights and moments are
+        the caller's tensors).  After graph-capturable steps, call
+        pull_groups first: their step counts live on the device."""
+        groups = []
+        for q in range(self._ngroups):
+            g = self.get_group(q)
+            groups.append(dict(lr=g["lr"], betas=list(g["betas"]), eps=g["eps"], weight_decay=g["weight_decay"],
+                               divisor=self.get_group_divisor(q), step=self.get_group_step(q)))
+        return {"groups": groups}  # plain numbers and lists: JSON round-trips it unchanged
+
+    def load_state_dict(self, state: dict):
+        """Restore state_dict() output: creates the groups on a handle that
+        has none, else overwrites as many groups as it has (the counts must
+        match).  Before graph-capturable steps, call push_groups after this."""
+        groups = state["groups"]
+        if self._ngroups == 0:
+            for g in groups:
+                self.add_group(g["lr"], tuple(g["betas"]), g["eps"], g["weight_decay"])
+        elif self._ngroups != len(groups):
+            raise ValueError(f"state has {len(groups)} groups, this handle {self._ngroups}")
+        for q, g in enumerate(groups):
+            self.set_group(q, g["lr"], tuple(g["betas"]), g["eps"], g["weight_decay"])
+            self.set_group_divisor(q, g["divisor"])
+            self.set_group_step(q, int(g["step"]))
 
     def set_lr(self, group: int, lr: float):
         self._check(_abi.soma_opt_set_lr(self._h, group, lr))

@@ -304,3 +304,27 @@ def test_cache_stats_of_a_fresh_handle_and_after_a_failed_step():
     assert opt.cache_stats() == {"builds": 0, "reuses": 0, "entries": 0}
     assert _abi.soma_opt_get_cache_stats(opt.handle, None, None, None) == _abi.SOMA_OK
     opt.close()
+
+
+def test_state_dict_round_trip():
+    # The library's whole state (group hyperparameters, divisors, step
+    # counts) survives a checkpoint into a fresh handle; no GPU needed.
+    import json
+    a = SomaOpt(0)
+    a.add_group(lr=1e-3, betas=(0.8, 0.99), eps=1e-6, weight_decay=0.1)
+    a.add_group(lr=5e-6)
+    a.set_group_divisor(1, 3.0)
+    a.set_group_step(0, 1234)
+    a.set_group_step(1, 7)
+    state = json.loads(json.dumps(a.state_dict()))  # as a checkpoint file would hold it
+    b = SomaOpt(0)
+    b.load_state_dict(state)
+    assert b.num_groups == 2
+    assert b.state_dict() == state
+    assert b.get_group_step(0) == 1234 and b.get_group_divisor(1) == 3.0
+    c = SomaOpt(0)
+    c.add_group(lr=1.0)
+    with pytest.raises(ValueError):
+        c.load_state_dict(state)
+    for o in (a, b, c):
+        o.close()
