@@ -25,7 +25,7 @@
 namespace {
 
 constexpr int32_t kDefaultUpdateChunk = 16384;
-constexpr int32_t kDefaultNormChunk = 131072;
+constexpr int32_t kDefaultNormChunk = 114688;  // 112 Ki: same-box sweeps of 64-192 Ki put it best or within noise
 constexpr int64_t kMinAutoChunk = 1024;   // smallest chunk the automatic sizing picks
 constexpr int64_t kAutoChunksPerSm = 4;   // small lists: aim for this many chunks per SM
 constexpr size_t kTimingRing = 1024;
