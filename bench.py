@@ -166,11 +166,37 @@ def describe(w):
     }
 
 
+def _code_only(text):
+    """C++ source without comments and with whitespace collapsed (string
+    literals kept): a comment edit leaves the hash of the code unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            i = text.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash():
+    """Hash of the kernels' code (comments and layout ignored): the ncu
+    traffic record applies only to the code it was measured on."""
     h = hashlib.sha256()
     for f in ("kernels.cu", "soma_kernels.h"):
-        with open(os.path.join(ROOT, "tensor_grad_clip_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tensor_grad_clip_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

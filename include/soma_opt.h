@@ -3,8 +3,8 @@
  * optimizer step for GB300 (sm_103a).
  *
  * What one step computes (SomaSpeed page, "Robot learning, at a different
- * pace", optimizer paragraphs "After backward, each trainable tensor has a
- * gradient ..." and "SomaSpeed batches that work across tensors ..."):
+ * pace", its two optimizer paragraphs: the first lists what a step does to
+ * each gradient, the second how the work is batched over the tensor list):
  *
  *   over a list of tensors, with d = grad_divisor (or the tensor's group
  *   divisor, see soma_opt_set_group_divisor),
@@ -158,7 +158,7 @@ soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n
 
 /* ---- graph-capturable step -------------------------------------------------
  * The SomaSpeed page replays repeated learner work with CUDA graphs to cut
- * launch overhead (its paragraph on compatible learner executions).  This
+ * launch overhead (its paragraph on replaying repeated learner work).  This
  * variant of soma_opt_step can be captured in a CUDA graph and replayed: it
  * enqueues only the two kernels, which read each group's hyperparameters and
  * step count from a table in device memory and advance the step counts there
@@ -204,8 +204,8 @@ soma_status_t soma_opt_device_groups(soma_opt_t opt, soma_device_group_t **table
 
 /* ---- multi-rank step (shard groups) -----------------------------------------
  * With FSDP/HSDP each rank owns some shards; the SomaSpeed page takes one
- * global clipping decision in which every shard counts once (its optimizer
- * paragraph "SomaSpeed batches that work across tensors ...").  The only data
+ * global clipping decision in which every shard counts once (its second
+ * optimizer paragraph, on batching the work over the tensor list).  The only data
  * the ranks exchange is one double per rank:
  *
  *   1. soma_opt_sumsq: this rank's sum over its trainable, owned entries of

@@ -6,8 +6,8 @@
  * does, and this file shares no code, header or constant with it.
  *
  * What it computes (SomaSpeed page, "Robot learning, at a different pace",
- * the two optimizer paragraphs "After backward, each trainable tensor has a
- * gradient ..." and "SomaSpeed batches that work across tensors ..."):
+ * its two optimizer paragraphs: the first lists what a step does to each
+ * gradient, the second how the work is batched over the tensor list):
  *
  *   1. normalize every gradient for the effective batch: g / d, where d is
  *      the step's divisor or, if its group sets one, the group's own (the

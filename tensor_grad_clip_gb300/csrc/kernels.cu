@@ -8,8 +8,8 @@
 //                   in fp64 in a fixed order, so the norm is the same bits
 //                   on every run whatever the CTA schedule, then derives
 //                   norm = sqrt(S) * (1/d) and c = min(1, max_norm/(norm + 1e-6)).
-//                   This is the "statistics needed for one global clipping
-//                   decision" of the SomaSpeed optimizer paragraphs, with
+//                   It gathers what the SomaSpeed optimizer paragraphs need
+//                   for one clipping decision over the whole list, with
 //                   ownership resolved by the host (only owned segments are
 //                   in this table).
 //

@@ -10,8 +10,8 @@
 //     tensor -- grouped into chunks of about the same number of elements.
 //     One CTA processes one chunk at a time.  Small tensors share a chunk,
 //     large tensors are cut into several; so one launch covers the whole
-//     list however many tensors it has (the "many small tensors" case of the
-//     SomaSpeed optimizer paragraphs).
+//     list however many tensors it has (the case of many small tensors that
+//     the SomaSpeed optimizer paragraphs single out).
 //
 // Vector body: inside a segment, elements [head, head + 8*nvec) are processed
 // eight at a time with 16-byte accesses, or 32-byte ones for fp32 buffers

@@ -1,8 +1,8 @@
 """The optimizer step over a shard group (FSDP/HSDP ranks).
 
 Every rank owns some shards; the SomaSpeed page takes one global clipping
-decision in which each gradient shard counts once (optimizer paragraph
-"SomaSpeed batches that work across tensors ...").  The ranks exchange one
+decision in which each gradient shard counts once (its second optimizer
+paragraph, on batching the work over the tensor list).  The ranks exchange one
 float64 each: their owned square-sum.
 
     step = ShardedStep(opt, group)           # after torch.distributed init

@@ -1,8 +1,8 @@
 """Write tests/golden/three_tensor_steps.txt from the fp64 oracle alone.
 
 The fixture is a worked example of the step the SomaSpeed page describes in
-its optimizer paragraphs ("After backward, each trainable tensor has a
-gradient ..." / "SomaSpeed batches that work across tensors ..."):
+its two optimizer paragraphs (what a step does to each gradient, and how
+the work is batched over the tensor list):
 normalize by the effective-batch divisor, one global norm over owned
 gradients, one clip coefficient, AdamW on every trainable tensor, frozen
 tensors untouched.  Inputs are short dyadic numbers (exact in fp32 and bf16);

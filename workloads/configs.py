@@ -5,8 +5,8 @@ hyperparameters and the random values of weights and gradients.  It holds
 none of the step's arithmetic, so the CUDA path and the fp64 oracle can both
 take their inputs from here without sharing any of the method.
 
-The five full-size workloads follow the optimizer paragraph of the SomaSpeed
-page ("After backward, each trainable tensor has a gradient ...") and the
+The five full-size workloads follow the SomaSpeed page's first optimizer
+paragraph (what a step does to each gradient) and the
 RLinf mixed-precision section ("Retaining Low-Precision Gradients": bf16
 gradients on fp32 state).  Unstated hyperparameters take the PPO settings of
 the veRL write-up ("Training Configuration": lr 5e-6, grad_clip 1) and
