@@ -62,7 +62,7 @@ def sample_indices(numel, seed, k):
     return np.unique(np.concatenate([head, tail, rand]))
 
 
-def run_full(w, steps, extra_idx=None):
+def run_full(w, steps, extra_idx=None, graph=False):
     dev = torch.device("cuda", 0)
     fb = W.FlatBuffers(w, dev, grad_step=1)
     opt = SomaOpt(0)
@@ -80,6 +80,8 @@ def run_full(w, steps, extra_idx=None):
         p0 = fb.p[k][ix_t].double().cpu().numpy()
         state.append([p0.copy(), np.zeros_like(p0), np.zeros_like(p0)])
     pool = ThreadPoolExecutor(16)
+    stream = torch.cuda.Stream() if graph else None
+    cuda_graph = torch.cuda.CUDAGraph() if graph else None
     for s in range(1, steps + 1):
         if s > 1:
             fb.load_grads(s)
@@ -88,8 +90,21 @@ def run_full(w, steps, extra_idx=None):
             opt.set_lr(q, lr)
         gbits = torch.int16 if fb.grad_dtype == torch.bfloat16 else torch.int32
         g_before = fb.G.view(gbits).clone()
-        opt.step(tl, w.grad_divisor, w.max_norm)
-        norm, coef, nonfinite = opt.get_norm()
+        if graph:  # captured once, replayed with the lr pushed each step
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                opt.push_groups(stream)
+                if s == 1:
+                    opt.step_graph(tl, w.grad_divisor, w.max_norm, stream)
+                    with torch.cuda.graph(cuda_graph, stream=stream):
+                        opt.step_graph(tl, w.grad_divisor, w.max_norm, stream)
+                else:
+                    cuda_graph.replay()
+            norm, coef, nonfinite = opt.get_norm(stream)
+            torch.cuda.current_stream().wait_stream(stream)
+        else:
+            opt.step(tl, w.grad_divisor, w.max_norm)
+            norm, coef, nonfinite = opt.get_norm()
         rn = oracle_norm(w, fb, w.grad_divisor, pool)
         rc = oracle.clip_coef(rn, w.max_norm)
         assert not nonfinite
@@ -108,6 +123,9 @@ def run_full(w, steps, extra_idx=None):
             assert_close(f"step {s} {t.name} p", fb.p[k][idx[k]].cpu().numpy(), p_s)
             assert_close(f"step {s} {t.name} m", fb.m[k][idx[k]].cpu().numpy(), m_s)
             assert_close(f"step {s} {t.name} v", fb.v[k][idx[k]].cpu().numpy(), v_s)
+    if graph:
+        opt.pull_groups(stream)
+        del cuda_graph
     for q in range(len(w.groups)):
         assert opt.get_group_step(q) == steps
     torch.cuda.synchronize()
@@ -126,6 +144,16 @@ def test_full_size_parity(name):
     plan = run_full(w, steps=10)
     assert plan["trainable_numel"] == w.trainable_numel
     assert plan["owned_numel"] == w.owned_numel
+
+
+def test_full_size_graph_replays():
+    # The graph-capturable step at full size: one capture, replays with the
+    # lr pushed each step (the flat list's cosine schedule), sampled against
+    # the oracle like the regular step.
+    w = W.with_steps(W.FULL["flat"](), 4)
+    run_full(w, steps=4, graph=True)
+    w = W.with_steps(W.FULL["action_expert"](), 3)
+    run_full(w, steps=3, graph=True)
 
 
 def test_tensor_beyond_2_pow_31_elements():
