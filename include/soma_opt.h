@@ -162,7 +162,7 @@ soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n
  * variant of soma_opt_step can be captured in a CUDA graph and replayed: it
  * enqueues only the two kernels, which read each group's hyperparameters and
  * step count from a table in device memory and advance the step counts there
- * (the square-sum kernel's last CTA does it, right after deriving c).
+ * (one extra CTA of the square-sum kernel does it while the others stream).
  * grad_divisor, max_norm and the group divisors become part of a captured
  * graph.
  *
@@ -171,7 +171,10 @@ soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n
  * on the handle keeps that list and its launch plan for its lifetime (other
  * lists and soma_opt_set_tuning fail with SOMA_ERR_STATE; use another handle),
  * so a captured graph never sees its tables move.  The host copy of the step
- * counts is not advanced; soma_opt_pull_groups refreshes it. */
+ * counts is not advanced; soma_opt_pull_groups refreshes it.  To mix the two
+ * kinds of step on one handle, call soma_opt_pull_groups before a regular step
+ * that follows graph steps, and soma_opt_push_groups before graph steps that
+ * follow regular ones. */
 soma_status_t soma_opt_step_graph(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
                                   double grad_divisor, double max_norm, void *stream);
 
