@@ -196,3 +196,41 @@ def test_regular_and_multirank_steps_refuse_stream_capture():
     opt.step(dl.tl, w.grad_divisor, w.max_norm)  # still usable outside capture
     assert opt.get_group_step(0) == 2
     opt.close()
+
+
+def test_regular_and_graph_steps_mixed_on_one_handle():
+    # The documented rule: push_groups before graph steps that follow regular
+    # ones, pull_groups before regular steps that follow graph steps.  Every
+    # step is compared with the oracle.
+    w = W.with_steps(W.SMALL["hsdp_shard"](), 6)
+    params = W.draw_params(w, "cpu")
+    dl = DeviceList(w, params)
+    opt = make_opt(w)
+    orc = make_oracle(w, params)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    for s in range(1, w.steps + 1):
+        grads = W.draw_grads(w, s, "cpu")
+        dl.load_grads(grads)
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            if s in (1, 2, 5, 6):  # regular steps
+                if s == 5:
+                    opt.pull_groups(stream)
+                opt.step(dl.tl, w.grad_divisor, w.max_norm, stream)
+            else:  # graph steps 3 and 4
+                if s == 3:
+                    opt.push_groups(stream)
+                    opt.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)  # step 3, outside capture
+                    with torch.cuda.graph(graph, stream=stream):
+                        opt.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)
+                else:
+                    graph.replay()  # step 4
+        norm, coef, _ = opt.get_norm(stream)
+        torch.cuda.current_stream().wait_stream(stream)
+        rn, rc = orc.step(grads, w.grad_divisor, w.max_norm)
+        assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (s, norm, rn)
+        _check_state(w, dl, orc, s)
+    assert [opt.get_group_step(q) for q in range(len(w.groups))] == [6] * len(w.groups)
+    del graph
+    opt.close()
