@@ -70,7 +70,7 @@ typedef int32_t soma_status_t;
 #define SOMA_DTYPE_F16   2  /* IEEE binary16 */
 
 #define SOMA_MAX_GROUPS  64
-#define SOMA_ABI_VERSION 3
+#define SOMA_ABI_VERSION 4
 
 typedef struct soma_opt soma_opt;
 typedef soma_opt *soma_opt_t;
@@ -147,7 +147,10 @@ soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
  * finite.  Each group with at least one trainable entry in the list advances
  * its step count by one.  Enqueues two kernels on `stream` and returns without
  * waiting for them: the owned square-sum (which also derives norm and c on
- * the device) and the fused update.  No device-to-host synchronisation
+ * the device) and the fused update.  A list small enough for the single-launch
+ * step (soma_opt_set_single_launch) runs as one kernel instead, one thread-
+ * block cluster, with the same results bit for bit, unless kernel timing is on
+ * or a group of the list sets its own divisor.  No device-to-host synchronisation
  * happens, except that a list the handle has not prepared yet waits for the
  * previous step's kernels before its device tables are written (see the
  * prepared-list cache below).  The group constants are fixed when the step is
@@ -163,6 +166,8 @@ soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n
  * enqueues only the two kernels, which read each group's hyperparameters and
  * step count from a table in device memory and advance the step counts there
  * (one extra CTA of the square-sum kernel does it while the others stream).
+ * A list small enough for the single-launch step runs as that one kernel here
+ * too, its CTAs deriving the group constants themselves.
  * grad_divisor, max_norm and the group divisors become part of a captured
  * graph.
  *
@@ -247,13 +252,15 @@ soma_status_t soma_opt_read_timing(soma_opt_t opt, double *norm_ms, double *upda
                                    int64_t *steps);
 
 /* Launch plan of the last step: chunk and segment counts, grid and block
- * sizes of the square-sum and update kernels.  Any pointer may be NULL. */
+ * sizes of the square-sum and update kernels, the kernels the last step
+ * launched, and single_launch_ctas: the CTAs of its one cluster when it ran
+ * as the single-launch step, else 0.  Any pointer may be NULL. */
 typedef struct {
     int64_t norm_chunks, norm_segments, update_chunks, update_segments;
     int32_t norm_grid, norm_block, update_grid, update_block;
     int64_t trainable_numel, owned_numel;
     int32_t launches_per_step;
-    int32_t reserved;
+    int32_t single_launch_ctas;
 } soma_plan_t;
 soma_status_t soma_opt_get_plan(soma_opt_t opt, soma_plan_t *plan);
 
@@ -280,6 +287,23 @@ soma_status_t soma_opt_get_cache_stats(soma_opt_t opt, int64_t *builds, int64_t 
  * effect at the next list (re)build. */
 soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t norm_chunk,
                                   int32_t update_ctas_per_sm, int32_t norm_ctas_per_sm);
+
+/* Single-launch step for small lists.  For a list of at most max_elements
+ * trainable elements, a regular step is one kernel: one thread-block cluster
+ * (16 CTAs where the device can run such a cluster, else 8, 4 or 2) whose CTAs
+ * square-sum their share of the norm chunks, meet at the hardware cluster
+ * barrier, each add all chunk sums in the fixed order of the two-kernel path
+ * (so each derives the same c), and update their share of the list.  The
+ * chain of two dependent kernels costs more than the work of such a list.
+ * Such lists are cut into about one chunk per CTA in both tables (unless
+ * soma_opt_set_tuning fixed the chunk sizes), and the two-kernel path (timed
+ * steps, graph steps, group divisors, the multi-rank step) uses the same
+ * tables, so every path gives the same bits.  max_elements: -1 = automatic
+ * (4096 per CTA of the cluster, one 8-element vector per thread: 65536 with
+ * 16 CTAs; larger lists ran faster as two kernels on GB300), 0 = never.  Drops the
+ * prepared lists like soma_opt_set_tuning, and like it fails with
+ * SOMA_ERR_STATE on a handle that ran a graph-capturable step. */
+soma_status_t soma_opt_set_single_launch(soma_opt_t opt, int64_t max_elements);
 
 /* Text of a status code (static storage). */
 const char *soma_status_string(soma_status_t status);

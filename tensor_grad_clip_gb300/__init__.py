@@ -280,7 +280,7 @@ class SomaOpt:
     def plan(self) -> dict:
         p = soma_plan_t()
         self._check(_abi.soma_opt_get_plan(self._h, ctypes.byref(p)))
-        return {name: getattr(p, name) for name, _ in soma_plan_t._fields_ if name != "reserved"}
+        return {name: getattr(p, name) for name, _ in soma_plan_t._fields_}
 
     def cache_stats(self) -> dict:
         """Prepared-list cache: table builds, steps that reused a prepared
@@ -293,6 +293,11 @@ class SomaOpt:
                    norm_ctas_per_sm: int = 0):
         self._check(_abi.soma_opt_set_tuning(self._h, update_chunk, norm_chunk, update_ctas_per_sm,
                                              norm_ctas_per_sm))
+
+    def set_single_launch(self, max_elements: int = -1):
+        """Regular steps of lists with at most max_elements trainable elements
+        run as one kernel (one thread-block cluster); -1 = automatic, 0 = never."""
+        self._check(_abi.soma_opt_set_single_launch(self._h, max_elements))
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

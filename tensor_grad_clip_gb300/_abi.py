@@ -24,7 +24,7 @@ SOMA_DTYPE_F32 = 0
 SOMA_DTYPE_BF16 = 1
 SOMA_DTYPE_F16 = 2
 SOMA_MAX_GROUPS = 64
-SOMA_ABI_VERSION = 3
+SOMA_ABI_VERSION = 4
 SOMA_MAX_RANKS = 65536
 SOMA_PLAN_CACHE = 4
 
@@ -64,7 +64,7 @@ class soma_plan_t(ctypes.Structure):
         ("trainable_numel", ctypes.c_int64),
         ("owned_numel", ctypes.c_int64),
         ("launches_per_step", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("single_launch_ctas", ctypes.c_int32),
     ]
 
 
@@ -102,6 +102,7 @@ SIGNATURES = {
     "soma_opt_get_plan": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_plan_t)]),
     "soma_opt_get_cache_stats": (soma_status_t, [soma_opt_t, _I64P, _I64P, _I32P]),
     "soma_opt_set_tuning": (soma_status_t, [soma_opt_t, _I32, _I32, _I32, _I32]),
+    "soma_opt_set_single_launch": (soma_status_t, [soma_opt_t, _I64]),
     "soma_status_string": (ctypes.c_char_p, [soma_status_t]),
     "soma_opt_last_error": (ctypes.c_char_p, [soma_opt_t]),
     "soma_abi_version": (_I32, []),

@@ -1,4 +1,4 @@
-// The two kernels of one optimizer step (sm_103a).
+// The kernels of one optimizer step (sm_103a).
 //
 //  norm_kernel   -- owned square-sum.  Every CTA walks chunks of the norm
 //                   table, sums g^2 of its chunk in fp32 (per-thread
@@ -19,7 +19,13 @@
 //                   g (2 or 4 B) and p, m, v (4 B each) in, p, m, v out.
 //                   Gradients are never written.
 //
-// Both kernels are HBM-bound streams (about 0.5 flop per byte); they use 16-
+//  small_step_kernel -- both of the above in one launch for small lists: one
+//                   thread-block cluster whose CTAs meet at the hardware
+//                   cluster barrier between the square-sum and the update,
+//                   with the same per-chunk code and the same fixed-order
+//                   sum, hence the same bits.
+//
+// The kernels are HBM-bound streams (about 0.5 flop per byte); they use 16-
 // and 32-byte vector accesses and no tensor cores.  Consecutive kernels of a
 // step, and of consecutive steps, overlap by programmatic dependent launch:
 // each kernel signals griddepcontrol.launch_dependents at its start, and the
@@ -315,6 +321,39 @@ __device__ __noinline__ GroupHp group_constants(const DevGroup& g, int64_t t) {
     return make_group_hp(g.lr, g.beta1, g.beta2, g.eps, g.weight_decay, t);
 }
 
+// Square-sum of one staged norm chunk over the whole CTA (fp32 per-thread
+// sums, then the fixed-shape block tree); the total is valid in thread 0.
+__device__ __forceinline__ float chunk_square_sum(const Seg* segs, int ns, int* upre, int* spre, float* wsum) {
+    float a0 = 0.f, a1 = 0.f;
+    if (ns == 1) {
+        if (segs[0].gdtype == kBF16) segment_sumsq<kBF16>(segs[0], a0, a1);
+        else if (segs[0].gdtype == kF16) segment_sumsq<kF16>(segs[0], a0, a1);
+        else segment_sumsq<kF32>(segs[0], a0, a1);
+    } else {
+        segment_prefix<true>(segs, ns, upre, spre);
+        chunk_sumsq(segs, upre, spre, a0, a1);
+    }
+    return block_sum<kNormBlock>(a0 + a1, wsum);
+}
+
+// The n chunk partials added in one fixed order: thread t adds partials t,
+// t + B, t + 2B, ... (B = block size), eight loads in flight at a time, then
+// a fixed-shape block tree.  The total is valid in thread 0.
+__device__ __forceinline__ double partials_sum(const double* partials, int n, double* wsum64) {
+    double s = 0.0;
+    const int B = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + 7 * B < n; i += 8 * B) {
+        double x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = __ldcg(partials + i + u * B);
+        // pairwise: three dependent fp64 adds rather than eight
+        s += ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+    }
+    for (; i < n; i += B) s += __ldcg(partials + i);
+    return block_sum64<kNormBlock>(s, wsum64);
+}
+
 // kGroupDiv: some group has its own divisor.  Each norm chunk then belongs to
 // one group, and its partial is scaled by that group's 1/d^2; otherwise the
 // partials are raw sums of g^2 and the step's d is applied to the total.
@@ -353,16 +392,7 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
     }
     for (int c = first; c >= 0 && c < a.t.nchunks; c += stride) {
         const int ns = c == first ? ns0 : stage_segments(a.t, c, segs);
-        float a0 = 0.f, a1 = 0.f;
-        if (ns == 1) {
-            if (segs[0].gdtype == kBF16) segment_sumsq<kBF16>(segs[0], a0, a1);
-            else if (segs[0].gdtype == kF16) segment_sumsq<kF16>(segs[0], a0, a1);
-            else segment_sumsq<kF32>(segs[0], a0, a1);
-        } else {
-            segment_prefix<true>(segs, ns, upre, spre);
-            chunk_sumsq(segs, upre, spre, a0, a1);
-        }
-        const float bs = block_sum<kNormBlock>(a0 + a1, wsum);
+        const float bs = chunk_square_sum(segs, ns, upre, spre, wsum);
         if (threadIdx.x == 0) {
             if (kGroupDiv) {
                 const double w = a.inv_divisor[segs[0].group];
@@ -384,20 +414,7 @@ __global__ void __launch_bounds__(kNormBlock, 3) norm_kernel(const __grid_consta
     if (!last) return;
     __threadfence();
 
-    // Thread t adds partials t, t + B, t + 2B, ... in that order (B = block
-    // size), eight loads in flight at a time; then a fixed-shape tree.
-    double s = 0.0;
-    const int n = a.t.nchunks, B = blockDim.x;
-    int i = threadIdx.x;
-    for (; i + 7 * B < n; i += 8 * B) {
-        double x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __ldcg(a.partials + i + u * B);
-        // pairwise: three dependent fp64 adds rather than eight
-        s += ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-    }
-    for (; i < n; i += B) s += __ldcg(a.partials + i);
-    s = block_sum64<kNormBlock>(s, wsum64);
+    const double s = partials_sum(a.partials, a.t.nchunks, wsum64);
     if (threadIdx.x == 0) {
         const double norm = kGroupDiv ? sqrt(s) : sqrt(s) * a.inv_step_divisor;
         const double coef = clip_coefficient(norm, a.max_norm);
@@ -799,6 +816,181 @@ __global__ void __launch_bounds__(kUpdateBlock, 2) update_kernel(const __grid_co
     }
 }
 
+// Stages chunk ca of table ta into sa and chunk cb of tb into sb (a negative
+// chunk: none) with the loads of both in flight together; returns the
+// segment counts in na and nb.
+__device__ __forceinline__ void stage_two(const Table& ta, int ca, Seg* sa, int& na, const Table& tb, int cb,
+                                          Seg* sb, int& nb) {
+    constexpr int kWords = sizeof(Seg) / sizeof(uint4);
+    int ba = 0, ea = 0, bb = 0, eb = 0;
+    if (ca >= 0) {
+        ba = __ldg(ta.chunk_begin + ca);
+        ea = __ldg(ta.chunk_begin + ca + 1);
+    }
+    if (cb >= 0) {
+        bb = __ldg(tb.chunk_begin + cb);
+        eb = __ldg(tb.chunk_begin + cb + 1);
+    }
+    na = ea - ba;
+    nb = eb - bb;
+    const uint4* srca = reinterpret_cast<const uint4*>(ta.segs + ba);
+    const uint4* srcb = reinterpret_cast<const uint4*>(tb.segs + bb);
+    uint4* dsta = reinterpret_cast<uint4*>(sa);
+    uint4* dstb = reinterpret_cast<uint4*>(sb);
+    for (int i = threadIdx.x; i < kWords * (na + nb); i += blockDim.x) {
+        if (i < kWords * na) dsta[i] = __ldg(srca + i);
+        else dstb[i - kWords * na] = __ldg(srcb + (i - kWords * na));
+    }
+    __syncthreads();
+}
+
+// partials_sum for n <= 32, in warp 0: the same total, because every term
+// partials_sum adds beyond these 32 lanes' values is an exact +0 (each
+// thread's sum starts at 0.0, and the other warps' sums are +0).
+__device__ __forceinline__ double partials_sum_warp(const double* partials, int n) {
+    double x = 0.0;
+    if ((int)threadIdx.x < n) x = 0.0 + __ldcg(partials + threadIdx.x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// The whole step in one launch, for lists so small that the chain of two
+// dependent kernels costs more than their work: one thread-block cluster of K
+// CTAs (the grid is that one cluster).  CTA r square-sums norm chunks r,
+// r + K, ... with the square-sum kernel's per-chunk code, so the partials are
+// the same bits.  The hardware cluster barrier (release / acquire) then makes
+// every partial visible to every CTA: no CTA polls memory.  Each CTA adds all
+// partials in the square-sum kernel's fixed order, so all derive the same c
+// and scale as that kernel's last CTA would; CTA 0 publishes norm and c.
+// Then CTA r updates update chunks r, r + K, ... with the update kernel's
+// per-element code.  The first update chunk's vectors, when there is at most
+// one per thread, are loaded before the barrier: they do not depend on c.
+// One divisor only.  kGraph: the graph-capturable step; each CTA derives the
+// group constants from the device group table (warp 1, while warp 0 adds the
+// partials) from the step counts it read before the barrier, and CTA 0 writes
+// the advanced counts back after it.
+template <bool kGraph>
+__global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_constant__ NormArgs na,
+                                                                   const __grid_constant__ UpdateArgs ua) {
+    __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];   // norm chunk, later update chunks
+    __shared__ __align__(16) Seg usegs[kMaxSegsPerChunk];  // the first update chunk
+    __shared__ int upre[kMaxSegsPerChunk + 1], spre[kMaxSegsPerChunk + 1];
+    __shared__ int vpre[kMaxSegsPerChunk + 1], vspre[kMaxSegsPerChunk + 1];
+    __shared__ float wsum[kNormBlock / 32];
+    __shared__ double wsum64[kNormBlock / 32];
+    __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
+
+    // The next step's launch may be scheduled once every CTA has started; it
+    // waits for this grid before touching anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int r = (int)blockIdx.x, K = (int)gridDim.x;
+    const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+    int ns0, nu0;
+    stage_two(na.t, r < na.t.nchunks ? r : -1, segs, ns0, ua.t, r < ua.t.nchunks ? r : -1, usegs, nu0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    Lane8 x;
+    int kx = -1;         // segment of this thread's early vector (vector index threadIdx.x), or none
+    bool early = false;  // the first update chunk's vectors are loaded
+    if (nu0 > 0) {
+        segment_prefix<false>(usegs, nu0, vpre, vspre);
+        const int V = vpre[kMaxSegsPerChunk];
+        if (V <= (int)blockDim.x) {
+            early = true;
+            const int v = threadIdx.x;
+            if (v < V) {
+                int k = 0;
+                while (v >= vpre[k + 1]) ++k;
+                load8(usegs[k], v - vpre[k], x);
+                kx = k;
+            }
+        }
+    }
+
+    // graph step: the step counts this step advances, read before the barrier
+    // (CTA 0 writes the new ones after it); lane l of warp 1 holds groups l, l + 32
+    int64_t t0 = 0, t1 = 0;
+    if (kGraph && warp == 1) {
+        if (lane < na.ngroups && ((na.present >> lane) & 1ull)) t0 = na.dgroups[lane].step + 1;
+        if (lane + 32 < na.ngroups && ((na.present >> (lane + 32)) & 1ull)) t1 = na.dgroups[lane + 32].step + 1;
+    }
+
+    for (int c = r; c < na.t.nchunks; c += K) {
+        const int ns = c == r ? ns0 : stage_segments(na.t, c, segs);
+        const float bs = chunk_square_sum(segs, ns, upre, spre, wsum);
+        if (threadIdx.x == 0) na.partials[c] = (double)bs;
+        __syncthreads();  // segs and wsum are reused by the next chunk
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+
+    double s = 0.0;
+    if (na.t.nchunks <= 32) {
+        if (threadIdx.x < 32) s = partials_sum_warp(na.partials, na.t.nchunks);
+    } else {
+        s = partials_sum(na.partials, na.t.nchunks, wsum64);
+    }
+    if (kGraph && warp == 1) {
+        if (t0 > 0) {
+            shp[lane] = group_constants(na.dgroups[lane], t0);
+            if (r == 0) na.dgroups[lane].step = t0;
+        }
+        if (t1 > 0) {
+            shp[lane + 32] = group_constants(na.dgroups[lane + 32], t1);
+            if (r == 0) na.dgroups[lane + 32].step = t1;
+        }
+    }
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(s) * na.inv_step_divisor;
+        const double coef = clip_coefficient(norm, na.max_norm);
+        const float scale = (float)(coef * na.inv_step_divisor);
+        if (r == 0) {
+            na.res->sumsq = s;
+            na.res->norm = norm;
+            na.res->coef = coef;
+            na.res->scale = scale;
+            na.res->nonfinite = isfinite(norm) ? 0u : 1u;
+            if (!isfinite(norm)) na.res->nonfinite_steps += 1u;
+        }
+        wsum[0] = scale;
+    }
+    __syncthreads();
+    const float scale = wsum[0];
+
+    int c0 = r;
+    if (early) {
+        if (kx >= 0) {
+            const Seg& sg = usegs[kx];
+            compute8(sg, x, kGraph ? shp[sg.group] : ua.groups[sg.group], scale);
+            store8(sg, (int)threadIdx.x - vpre[kx], x);
+        }
+        const int S = vspre[kMaxSegsPerChunk];
+        int k = 0;
+        for (int e = threadIdx.x; e < S; e += blockDim.x) {
+            while (e >= vspre[k + 1]) ++k;
+            const Seg& sg = usegs[k];
+            const int j = e - vspre[k];
+            update_one(sg, j < sg.head ? j : sg.head + kVec * sg.nvec + (j - sg.head),
+                       kGraph ? shp[sg.group] : ua.groups[sg.group], scale);
+        }
+        c0 = r + K;
+    }
+    for (int c = c0; c < ua.t.nchunks; c += K) {
+        const int ns = stage_segments(ua.t, c, segs);
+        if (ns == 1) {
+            const Seg& sg = segs[0];
+            const GroupHp& h = kGraph ? shp[sg.group] : ua.groups[sg.group];
+            if (sg.gdtype == kBF16) segment_update_low<kBF16>(sg, h, scale);
+            else if (sg.gdtype == kF16) segment_update_low<kF16>(sg, h, scale);
+            else segment_update_low<kF32>(sg, h, scale);
+        } else {
+            segment_prefix<false>(segs, ns, upre, spre);
+            chunk_update<kGraph, false>(segs, upre, spre, ua, shp, nullptr, scale);
+        }
+        __syncthreads();  // segs and the prefixes are rebuilt for the next chunk
+    }
+}
+
 }  // namespace
 
 int launch_norm(const NormArgs& a, int grid, void* stream, bool graph, bool group_div, bool overlap) {
@@ -837,6 +1029,55 @@ int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph, bool 
     else if (graph) e = cudaLaunchKernelEx(&cfg, update_kernel<true, false>, a);
     else if (group_div) e = cudaLaunchKernelEx(&cfg, update_kernel<false, true>, a);
     else e = cudaLaunchKernelEx(&cfg, update_kernel<false, false>, a);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaGetLastError();
+}
+
+int small_step_cluster_size() {
+    if (cudaFuncSetAttribute(small_step_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(small_step_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+    }
+    for (int k = kSmallStepMaxCtas; k >= 2; k /= 2) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(k);
+        cfg.blockDim = dim3(kNormBlock);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = k;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int plain = 0, graph = 0;
+        if (cudaOccupancyMaxActiveClusters(&plain, small_step_kernel<false>, &cfg) == cudaSuccess &&
+            cudaOccupancyMaxActiveClusters(&graph, small_step_kernel<true>, &cfg) == cudaSuccess && plain > 0 &&
+            graph > 0)
+            return k;
+        (void)cudaGetLastError();
+    }
+    return 0;
+}
+
+int launch_small_step(const NormArgs& na, const UpdateArgs& ua, int ctas, void* stream, bool overlap, bool graph) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kNormBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 2 : 1;
+    const cudaError_t e = graph ? cudaLaunchKernelEx(&cfg, small_step_kernel<true>, na, ua)
+                                : cudaLaunchKernelEx(&cfg, small_step_kernel<false>, na, ua);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }

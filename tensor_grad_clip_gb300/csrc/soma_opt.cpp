@@ -28,6 +28,7 @@ constexpr int32_t kDefaultUpdateChunk = 16384;
 constexpr int32_t kDefaultNormChunk = 114688;  // 112 Ki: same-box sweeps of 64-192 Ki put it best or within noise
 constexpr int64_t kMinAutoChunk = 1024;   // smallest chunk the automatic sizing picks
 constexpr int64_t kAutoChunksPerSm = 4;   // small lists: aim for this many chunks per SM
+constexpr int64_t kSinglePerCta = 4096;   // default single-launch limit: one 8-element vector per thread of each cluster CTA
 constexpr size_t kTimingRing = 1024;
 constexpr int kMaxPlans = SOMA_PLAN_CACHE;
 
@@ -62,6 +63,7 @@ struct PreparedList {
     soma::Table norm_tab{}, upd_tab{};
     std::vector<uint8_t> group_present;
     int norm_grid = 1, upd_grid = 0;
+    bool single = false;            // small enough for the single-launch step
     soma_plan_t info{};
 };
 
@@ -74,10 +76,12 @@ struct soma_opt {
     int32_t norm_chunk = 0;
     int32_t update_ctas_per_sm = 0; // 0: one CTA per chunk
     int32_t norm_ctas_per_sm = 0;
+    int64_t single_limit = -1;      // single-launch step up to this many trainable elements; -1: automatic
 
     // device state, created on first use
     bool dev_ready = false;
     int sm_count = 0;
+    int single_ctas = 0;            // CTAs (one cluster) of the single-launch step; 0: not available
     soma::Result* d_res = nullptr;
     soma::Result* h_res = nullptr;  // pinned
     double* d_partials = nullptr;
@@ -108,6 +112,7 @@ struct soma_opt {
     soma::Table norm_tab{}, upd_tab{};
     std::vector<uint8_t> group_present;
     int norm_grid = 1, upd_grid = 0;
+    bool single = false;
     soma_plan_t plan{};
 
     // kernel timing
@@ -273,6 +278,7 @@ soma_status_t ensure_device(soma_opt* o) {
     cudaError_t e;
     if ((e = cudaDeviceGetAttribute(&o->sm_count, cudaDevAttrMultiProcessorCount, o->device)) != cudaSuccess)
         return o->cuda_fail(e, "cudaDeviceGetAttribute");
+    o->single_ctas = soma::small_step_cluster_size();
     if ((e = cudaMalloc(&o->d_res, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMalloc(result)");
     if ((e = cudaMemset(o->d_res, 0, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMemset(result)");
     if ((e = cudaMallocHost(&o->h_res, sizeof(soma::Result))) != cudaSuccess) return o->cuda_fail(e, "cudaMallocHost");
@@ -322,6 +328,7 @@ void activate(soma_opt* o, int i) {
     o->group_present = pl.group_present;
     o->norm_grid = pl.norm_grid;
     o->upd_grid = pl.upd_grid;
+    o->single = pl.single;
     o->plan = pl.info;
 }
 
@@ -346,8 +353,19 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
         trainable_total += list[k].numel;
         if (list[k].owned) owned_total += list[k].numel;
     }
-    TableBuilder upd(chunk_size(o->update_chunk, kDefaultUpdateChunk, trainable_total, o->sm_count), false);
-    TableBuilder nrm(chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total, o->sm_count), true);
+    // A list for the single-launch step is cut into about one chunk per
+    // cluster CTA, so each CTA's share is one pass of its threads.
+    const int64_t limit = o->single_limit >= 0 ? o->single_limit : (int64_t)o->single_ctas * kSinglePerCta;
+    const bool single = o->single_ctas > 0 && trainable_total <= limit;
+    auto per_cta = [&](int64_t total) {
+        return std::max<int64_t>(64, (total + o->single_ctas - 1) / std::max(o->single_ctas, 1) + 63) / 64 * 64;
+    };
+    TableBuilder upd(o->update_chunk == 0 && single ? per_cta(trainable_total)
+                                                    : chunk_size(o->update_chunk, kDefaultUpdateChunk,
+                                                                 trainable_total, o->sm_count), false);
+    TableBuilder nrm(o->norm_chunk == 0 && single ? per_cta(owned_total)
+                                                  : chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total,
+                                                               o->sm_count), true);
     std::vector<uint8_t> present(o->groups.size(), 0);
     int64_t trainable = 0, owned = 0;
     for (int64_t k = 0; k < n; ++k) {
@@ -427,6 +445,7 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
     pl.upd_grid = (int)std::min<int64_t>(upd.nchunks(), ucap);
     pl.norm_grid = (int)std::max<int64_t>(1, std::min<int64_t>(nrm.nchunks(), ncap));
     pl.group_present = present;
+    pl.single = single;
     pl.key.assign(list, list + n);
 
     soma_plan_t& p = pl.info;
@@ -671,6 +690,17 @@ soma_status_t soma_opt_set_tuning(soma_opt_t h, int32_t update_chunk, int32_t no
     return SOMA_OK;
 }
 
+soma_status_t soma_opt_set_single_launch(soma_opt_t h, int64_t max_elements) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (max_elements < -1) return o->fail(SOMA_ERR_INVALID_ARG, "max_elements must be -1, 0 or positive");
+    if (o->graph_locked) return o->fail(SOMA_ERR_STATE, "this handle ran a graph-capturable step: its plan is fixed");
+    o->single_limit = max_elements;
+    for (auto& pl : o->plans) pl.valid = false;
+    o->active = -1;
+    return SOMA_OK;
+}
+
 namespace {
 
 // Does a group present in the active list set its own divisor?
@@ -736,6 +766,7 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
     host_group_constants(o, ua, next);
     cudaError_t e;
     soma_status_t st;
+    bool single = false;
     std::array<cudaEvent_t, 3>* ev = nullptr;
     if (o->timing) {
         if (o->tev_used == kTimingRing && (st = timing_flush(o)) != SOMA_OK) return st;
@@ -775,19 +806,27 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         fill_divisors(o, grad_divisor, na.inv_divisor);
         na.gscale = o->d_gscale;
         na.ngroups = (int32_t)o->groups.size();
-        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o),
-                                                ev == nullptr)) !=
-            cudaSuccess)
+        // Small lists run as one launch, unless timing events must separate
+        // the two kernels or some group sets its own divisor.
+        single = o->single && ev == nullptr && !any_group_divisor(o);
+        if (single) {
+            if ((e = (cudaError_t)soma::launch_small_step(na, ua, o->single_ctas, stream, true)) != cudaSuccess)
+                return o->cuda_fail(e, "launching the single-launch step");
+        } else if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o),
+                                                       ev == nullptr)) != cudaSuccess) {
             return o->cuda_fail(e, "launching the square-sum kernel");
+        }
     }
     if (ev && (e = cudaEventRecord((*ev)[1], (cudaStream_t)stream)) != cudaSuccess)
         return o->cuda_fail(e, "cudaEventRecord");
     // without a timing event between the two kernels, the update kernel may
     // overlap the square-sum kernel's tail
-    if (o->upd_grid > 0 &&
+    if (!single && o->upd_grid > 0 &&
         (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, false, ev == nullptr,
                                               any_group_divisor(o))) != cudaSuccess)
         return o->cuda_fail(e, "launching the update kernel");
+    o->plan.launches_per_step = single ? 1 : 1 + (o->upd_grid > 0 ? 1 : 0);
+    o->plan.single_launch_ctas = single ? o->single_ctas : 0;
     if (ev) {
         if ((e = cudaEventRecord((*ev)[2], (cudaStream_t)stream)) != cudaSuccess)
             return o->cuda_fail(e, "cudaEventRecord");
@@ -930,14 +969,22 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
     ua.dhp = o->d_hp;
     ua.ngroups = (int32_t)o->groups.size();
     ua.gscale = o->d_gscale;
-    // one CTA more than the chunks need: CTA 0 derives the group constants
-    if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid + 1, stream, true, any_group_divisor(o))) !=
-        cudaSuccess)
-        return o->cuda_fail(e, "launching the square-sum kernel");
-    if (o->upd_grid > 0 &&
-        (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true, true, any_group_divisor(o))) !=
+    const bool single = o->single && !any_group_divisor(o);
+    if (single) {
+        if ((e = (cudaError_t)soma::launch_small_step(na, ua, o->single_ctas, stream, true, true)) != cudaSuccess)
+            return o->cuda_fail(e, "launching the single-launch step");
+    } else {
+        // one CTA more than the chunks need: CTA 0 derives the group constants
+        if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid + 1, stream, true, any_group_divisor(o))) !=
             cudaSuccess)
-        return o->cuda_fail(e, "launching the update kernel");
+            return o->cuda_fail(e, "launching the square-sum kernel");
+        if (o->upd_grid > 0 &&
+            (e = (cudaError_t)soma::launch_update(ua, o->upd_grid, stream, true, true, any_group_divisor(o))) !=
+                cudaSuccess)
+            return o->cuda_fail(e, "launching the update kernel");
+    }
+    o->plan.launches_per_step = single ? 1 : 1 + (o->upd_grid > 0 ? 1 : 0);
+    o->plan.single_launch_ctas = single ? o->single_ctas : 0;
     o->graph_locked = true;
     if (!cap) {
         if ((e = cudaEventRecord(o->done, (cudaStream_t)stream)) != cudaSuccess)

@@ -157,7 +157,7 @@ def make_oracle(w: W.Workload, params_cpu) -> OracleOptimizer:
 
 
 def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=None, check_every_step=True,
-               tensor_rtol=0.0):
+               tensor_rtol=0.0, single_launch=None, expect_launches=None):
     """Chained steps of `w` on the GPU and in the oracle, compared after
     every step.  Returns the list of (gpu_norm, oracle_norm, gpu_coef,
     oracle_coef) per step.
@@ -167,13 +167,19 @@ def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=
     by about 2^-24 of its two terms, not of their difference: where they
     cancel, the element-relative bound cannot hold whatever the kernel does.
     The workloads' gradients keep the terms small enough that it does; lists
-    with large gradients need this term."""
+    with large gradients need this term.
+
+    single_launch: when set, the handle's single-launch limit
+    (soma_opt_set_single_launch); expect_launches: when set, the kernels every
+    step must have launched (1 = the single-launch step)."""
     steps = w.steps if steps is None else steps
     params = W.draw_params(w, "cpu")
     dl = DeviceList(w, params, shift=shift, frozen_null=frozen_null)
     opt = make_opt(w)
     if tuning:
         opt.set_tuning(**tuning)
+    if single_launch is not None:
+        opt.set_single_launch(single_launch)
     orc = make_oracle(w, params)
     out = []
     for s in range(1, steps + 1):
@@ -186,6 +192,8 @@ def run_parity(w: W.Workload, steps=None, shift=None, frozen_null=False, tuning=
         snap = dl.snapshot()
         opt.step(dl.tl, w.grad_divisor, w.max_norm)
         norm, coef, nonfinite = opt.get_norm()
+        if expect_launches is not None:
+            assert opt.plan()["launches_per_step"] == expect_launches, opt.plan()
         rn, rc = orc.step(grads, w.grad_divisor, w.max_norm)
         out.append((norm, rn, coef, rc))
         assert not nonfinite

@@ -36,6 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_layout():
+    assert ctypes.sizeof(_abi.soma_plan_t) == 72 and _abi.soma_plan_t.single_launch_ctas.offset == 68
     assert ctypes.sizeof(_abi.soma_tensor_t) == 56
     assert _abi.soma_tensor_t.param_lowp.offset == 32
     assert _abi.soma_tensor_t.numel.offset == 40 and _abi.soma_tensor_t.group.offset == 48
@@ -216,7 +217,11 @@ def test_tuning_and_timing_arguments():
     assert _abi.soma_opt_set_timing(opt.handle, 2) == _abi.SOMA_ERR_INVALID_ARG
     opt.set_timing(True)
     assert opt.read_timing() == (0.0, 0.0, 0)
+    for ok in (-1, 0, 1, 1 << 40):
+        opt.set_single_launch(ok)
+    assert _abi.soma_opt_set_single_launch(opt.handle, -2) == _abi.SOMA_ERR_INVALID_ARG
     opt.close()
+    assert _abi.soma_opt_set_single_launch(opt.handle, 0) == _abi.SOMA_ERR_STATE
 
 
 def test_tensor_list_marshalling_checks():
