@@ -149,8 +149,8 @@ soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
  * waiting for them: the owned square-sum (which also derives norm and c on
  * the device) and the fused update.  A list small enough for the single-launch
  * step (soma_opt_set_single_launch) runs as one kernel instead, one thread-
- * block cluster, with the same results bit for bit, unless kernel timing is on
- * or a group of the list sets its own divisor.  No device-to-host synchronisation
+ * block cluster, with the same results bit for bit, unless kernel timing is
+ * on.  No device-to-host synchronisation
  * happens, except that a list the handle has not prepared yet waits for the
  * previous step's kernels before its device tables are written (see the
  * prepared-list cache below).  The group constants are fixed when the step is
@@ -297,8 +297,8 @@ soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t 
  * chain of two dependent kernels costs more than the work of such a list.
  * Such lists are cut into about one chunk per CTA in both tables (unless
  * soma_opt_set_tuning fixed the chunk sizes), and the two-kernel path (timed
- * steps, graph steps, group divisors, the multi-rank step) uses the same
- * tables, so every path gives the same bits.  max_elements: -1 = automatic
+ * steps, the multi-rank step) uses the same tables, so every path gives the
+ * same bits.  max_elements: -1 = automatic
  * (4096 per CTA of the cluster, one 8-element vector per thread: 65536 with
  * 16 CTAs; larger lists ran faster as two kernels on GB300), 0 = never.  Drops the
  * prepared lists like soma_opt_set_tuning, and like it fails with

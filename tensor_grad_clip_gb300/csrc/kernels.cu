@@ -866,11 +866,13 @@ __device__ __forceinline__ double partials_sum_warp(const double* partials, int 
 // Then CTA r updates update chunks r, r + K, ... with the update kernel's
 // per-element code.  The first update chunk's vectors, when there is at most
 // one per thread, are loaded before the barrier: they do not depend on c.
-// One divisor only.  kGraph: the graph-capturable step; each CTA derives the
-// group constants from the device group table (warp 1, while warp 0 adds the
-// partials) from the step counts it read before the barrier, and CTA 0 writes
-// the advanced counts back after it.
-template <bool kGraph>
+// kGraph: the graph-capturable step; each CTA derives the group constants
+// from the device group table (warp 1, while warp 0 adds the partials) from
+// the step counts it read before the barrier, and CTA 0 writes the advanced
+// counts back after it.  kGroupDiv: some group sets its own divisor; as in
+// the two kernels, each partial is scaled by its chunk's group's 1/d^2 and
+// every CTA forms c/d of each group.
+template <bool kGraph, bool kGroupDiv>
 __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_constant__ NormArgs na,
                                                                    const __grid_constant__ UpdateArgs ua) {
     __shared__ __align__(16) Seg segs[kMaxSegsPerChunk];   // norm chunk, later update chunks
@@ -880,6 +882,7 @@ __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_
     __shared__ float wsum[kNormBlock / 32];
     __shared__ double wsum64[kNormBlock / 32];
     __shared__ GroupHp shp[kGraph ? kMaxGroups : 1];
+    __shared__ float gs[kGroupDiv ? kMaxGroups : 1];  // c / d of each group
 
     // The next step's launch may be scheduled once every CTA has started; it
     // waits for this grid before touching anything.
@@ -919,7 +922,14 @@ __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_
     for (int c = r; c < na.t.nchunks; c += K) {
         const int ns = c == r ? ns0 : stage_segments(na.t, c, segs);
         const float bs = chunk_square_sum(segs, ns, upre, spre, wsum);
-        if (threadIdx.x == 0) na.partials[c] = (double)bs;
+        if (threadIdx.x == 0) {
+            if (kGroupDiv) {
+                const double w = na.inv_divisor[segs[0].group];
+                na.partials[c] = (double)bs * w * w;
+            } else {
+                na.partials[c] = (double)bs;
+            }
+        }
         __syncthreads();  // segs and wsum are reused by the next chunk
     }
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -941,7 +951,7 @@ __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_
         }
     }
     if (threadIdx.x == 0) {
-        const double norm = sqrt(s) * na.inv_step_divisor;
+        const double norm = kGroupDiv ? sqrt(s) : sqrt(s) * na.inv_step_divisor;
         const double coef = clip_coefficient(norm, na.max_norm);
         const float scale = (float)(coef * na.inv_step_divisor);
         if (r == 0) {
@@ -953,15 +963,22 @@ __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_
             if (!isfinite(norm)) na.res->nonfinite_steps += 1u;
         }
         wsum[0] = scale;
+        wsum64[0] = coef;
     }
     __syncthreads();
     const float scale = wsum[0];
+    if (kGroupDiv) {
+        const double coef = wsum64[0];
+        for (int q = threadIdx.x; q < na.ngroups && q < kMaxGroups; q += blockDim.x)
+            gs[q] = (float)(coef * na.inv_divisor[q]);
+        __syncthreads();
+    }
 
     int c0 = r;
     if (early) {
         if (kx >= 0) {
             const Seg& sg = usegs[kx];
-            compute8(sg, x, kGraph ? shp[sg.group] : ua.groups[sg.group], scale);
+            compute8(sg, x, kGraph ? shp[sg.group] : ua.groups[sg.group], kGroupDiv ? gs[sg.group] : scale);
             store8(sg, (int)threadIdx.x - vpre[kx], x);
         }
         const int S = vspre[kMaxSegsPerChunk];
@@ -971,7 +988,7 @@ __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_
             const Seg& sg = usegs[k];
             const int j = e - vspre[k];
             update_one(sg, j < sg.head ? j : sg.head + kVec * sg.nvec + (j - sg.head),
-                       kGraph ? shp[sg.group] : ua.groups[sg.group], scale);
+                       kGraph ? shp[sg.group] : ua.groups[sg.group], kGroupDiv ? gs[sg.group] : scale);
         }
         c0 = r + K;
     }
@@ -980,12 +997,13 @@ __global__ void __launch_bounds__(kNormBlock, 1) small_step_kernel(const __grid_
         if (ns == 1) {
             const Seg& sg = segs[0];
             const GroupHp& h = kGraph ? shp[sg.group] : ua.groups[sg.group];
-            if (sg.gdtype == kBF16) segment_update_low<kBF16>(sg, h, scale);
-            else if (sg.gdtype == kF16) segment_update_low<kF16>(sg, h, scale);
-            else segment_update_low<kF32>(sg, h, scale);
+            const float sc = kGroupDiv ? gs[sg.group] : scale;
+            if (sg.gdtype == kBF16) segment_update_low<kBF16>(sg, h, sc);
+            else if (sg.gdtype == kF16) segment_update_low<kF16>(sg, h, sc);
+            else segment_update_low<kF32>(sg, h, sc);
         } else {
             segment_prefix<false>(segs, ns, upre, spre);
-            chunk_update<kGraph, false>(segs, upre, spre, ua, shp, nullptr, scale);
+            chunk_update<kGraph, kGroupDiv>(segs, upre, spre, ua, shp, gs, scale);
         }
         __syncthreads();  // segs and the prefixes are rebuilt for the next chunk
     }
@@ -1034,12 +1052,13 @@ int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph, bool 
 }
 
 int small_step_cluster_size() {
-    if (cudaFuncSetAttribute(small_step_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(small_step_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess) {
-        (void)cudaGetLastError();
-    }
+    const void* variants[4] = {reinterpret_cast<const void*>(small_step_kernel<false, false>),
+                               reinterpret_cast<const void*>(small_step_kernel<false, true>),
+                               reinterpret_cast<const void*>(small_step_kernel<true, false>),
+                               reinterpret_cast<const void*>(small_step_kernel<true, true>)};
+    for (const void* f : variants)
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            (void)cudaGetLastError();
     for (int k = kSmallStepMaxCtas; k >= 2; k /= 2) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(k);
@@ -1051,17 +1070,19 @@ int small_step_cluster_size() {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        int plain = 0, graph = 0;
-        if (cudaOccupancyMaxActiveClusters(&plain, small_step_kernel<false>, &cfg) == cudaSuccess &&
-            cudaOccupancyMaxActiveClusters(&graph, small_step_kernel<true>, &cfg) == cudaSuccess && plain > 0 &&
-            graph > 0)
-            return k;
+        bool all = true;
+        for (const void* f : variants) {
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, f, &cfg) != cudaSuccess || clusters <= 0) all = false;
+        }
+        if (all) return k;
         (void)cudaGetLastError();
     }
     return 0;
 }
 
-int launch_small_step(const NormArgs& na, const UpdateArgs& ua, int ctas, void* stream, bool overlap, bool graph) {
+int launch_small_step(const NormArgs& na, const UpdateArgs& ua, int ctas, void* stream, bool overlap, bool graph,
+                      bool group_div) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kNormBlock);
@@ -1076,8 +1097,11 @@ int launch_small_step(const NormArgs& na, const UpdateArgs& ua, int ctas, void* 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 2 : 1;
-    const cudaError_t e = graph ? cudaLaunchKernelEx(&cfg, small_step_kernel<true>, na, ua)
-                                : cudaLaunchKernelEx(&cfg, small_step_kernel<false>, na, ua);
+    cudaError_t e;
+    if (graph && group_div) e = cudaLaunchKernelEx(&cfg, small_step_kernel<true, true>, na, ua);
+    else if (graph) e = cudaLaunchKernelEx(&cfg, small_step_kernel<true, false>, na, ua);
+    else if (group_div) e = cudaLaunchKernelEx(&cfg, small_step_kernel<false, true>, na, ua);
+    else e = cudaLaunchKernelEx(&cfg, small_step_kernel<false, false>, na, ua);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }

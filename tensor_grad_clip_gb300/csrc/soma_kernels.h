@@ -204,14 +204,14 @@ int launch_update(const UpdateArgs& a, int grid, void* stream, bool graph = fals
                   bool group_div = false);
 int launch_finish(const FinishArgs& a, void* stream);
 
-// Single-launch step (small lists, one divisor): one cluster of `ctas` CTAs
-// does the square-sum, the norm and the update.  `ctas` must be a value
+// Single-launch step (small lists): one cluster of `ctas` CTAs does the
+// square-sum, the norm and the update.  `ctas` must be a value
 // small_step_cluster_size() returned.  overlap as above; graph = true takes
 // the group constants from NormArgs::dgroups and advances the step counts
-// there (UpdateArgs::groups unused).
+// there (UpdateArgs::groups unused); group_div as for launch_norm.
 constexpr int kSmallStepMaxCtas = 16;
 int small_step_cluster_size();  // largest cluster (16, 8, 4, 2) the device can run, else 0
 int launch_small_step(const NormArgs& na, const UpdateArgs& ua, int ctas, void* stream, bool overlap = false,
-                      bool graph = false);
+                      bool graph = false, bool group_div = false);
 
 }  // namespace soma

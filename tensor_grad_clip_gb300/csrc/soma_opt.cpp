@@ -807,10 +807,11 @@ soma_status_t launch_step(soma_opt* o, double grad_divisor, double max_norm, con
         na.gscale = o->d_gscale;
         na.ngroups = (int32_t)o->groups.size();
         // Small lists run as one launch, unless timing events must separate
-        // the two kernels or some group sets its own divisor.
-        single = o->single && ev == nullptr && !any_group_divisor(o);
+        // the two kernels.
+        single = o->single && ev == nullptr;
         if (single) {
-            if ((e = (cudaError_t)soma::launch_small_step(na, ua, o->single_ctas, stream, true)) != cudaSuccess)
+            if ((e = (cudaError_t)soma::launch_small_step(na, ua, o->single_ctas, stream, true, false,
+                                                          any_group_divisor(o))) != cudaSuccess)
                 return o->cuda_fail(e, "launching the single-launch step");
         } else if ((e = (cudaError_t)soma::launch_norm(na, o->norm_grid, stream, false, any_group_divisor(o),
                                                        ev == nullptr)) != cudaSuccess) {
@@ -969,9 +970,10 @@ soma_status_t soma_opt_step_graph(soma_opt_t h, const soma_tensor_t* list, int64
     ua.dhp = o->d_hp;
     ua.ngroups = (int32_t)o->groups.size();
     ua.gscale = o->d_gscale;
-    const bool single = o->single && !any_group_divisor(o);
+    const bool single = o->single;
     if (single) {
-        if ((e = (cudaError_t)soma::launch_small_step(na, ua, o->single_ctas, stream, true, true)) != cudaSuccess)
+        if ((e = (cudaError_t)soma::launch_small_step(na, ua, o->single_ctas, stream, true, true,
+                                                      any_group_divisor(o))) != cudaSuccess)
             return o->cuda_fail(e, "launching the single-launch step");
     } else {
         // one CTA more than the chunks need: CTA 0 derives the group constants

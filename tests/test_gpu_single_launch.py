@@ -114,10 +114,18 @@ def test_size_limit():
     run_parity(w, single_launch=0, expect_launches=2)
 
 
-def test_group_divisor_uses_two_kernels():
-    groups = (W.GroupSpec(lr=1e-3, weight_decay=0.01), W.GroupSpec(lr=2e-3, divisor=16.0))
-    w = _custom([T("a", (3000,)), T("b", (500,), W.BF16, group=1)], groups=groups)
-    run_parity(w, expect_launches=2)
+def test_group_divisors():
+    # each chunk's partial scaled by its group's 1/d^2, c/d per group: the
+    # oracle's results, and the two-kernel step's bits
+    groups = (W.GroupSpec(lr=1e-3, weight_decay=0.01), W.GroupSpec(lr=2e-3, divisor=16.0),
+              W.GroupSpec(lr=5e-4, divisor=0.5))
+    w = _custom([T("a", (3000,)), T("b", (500,), W.BF16, group=1), T("c", (20011,), group=2, param_lowp=W.BF16),
+                 T("d", (9,), W.F16, group=1, owned=False)], groups=groups)
+    run_parity(w, expect_launches=1)
+    one = _run(w)
+    two = _run(w, timing_at=range(1, w.steps + 1))
+    assert all(p["launches_per_step"] == 1 for p in one[1]) and all(p["launches_per_step"] == 2 for p in two[1])
+    _assert_same(one, two)
 
 
 def test_graph_steps_run_as_one_launch():
