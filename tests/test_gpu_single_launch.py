@@ -7,7 +7,7 @@ import torch
 
 import workloads as W
 from parity_harness import DeviceList, make_opt, run_parity
-from tensor_grad_clip_gb300 import build
+from tensor_grad_clip_gb300 import SomaError, _abi, build
 
 pytestmark = pytest.mark.gpu
 
@@ -150,3 +150,26 @@ def test_graph_steps_run_as_one_launch():
     state = [x.cpu().clone() for x in dl.p + dl.m + dl.v]
     opt.close()
     _assert_same(reg, (norms, plans, state))
+
+
+def test_limit_changes_drop_prepared_lists_and_graph_handles_refuse_them():
+    w = W.with_steps(W.SMALL["tiny"](), 1)
+    dl = DeviceList(w, W.draw_params(w, "cpu"))
+    dl.load_grads(W.draw_grads(w, 1, "cpu"))
+    opt = make_opt(w)
+    opt.step(dl.tl, w.grad_divisor, w.max_norm)
+    assert opt.cache_stats()["entries"] == 1 and opt.plan()["launches_per_step"] == 1
+    opt.set_single_launch(0)  # the tables are cut differently now: rebuilt at the next step
+    assert opt.cache_stats()["entries"] == 0
+    opt.step(dl.tl, w.grad_divisor, w.max_norm)
+    assert opt.plan()["launches_per_step"] == 2 and opt.cache_stats()["builds"] == 2
+    opt.close()
+    g = make_opt(w)
+    stream = torch.cuda.current_stream()
+    g.push_groups(stream)
+    g.step_graph(dl.tl, w.grad_divisor, w.max_norm, stream)
+    with pytest.raises(SomaError) as e:
+        g.set_single_launch(0)  # a captured graph may hold these tables
+    assert e.value.status == _abi.SOMA_ERR_STATE
+    torch.cuda.synchronize()
+    g.close()
