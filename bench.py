@@ -546,8 +546,9 @@ def run_ours(args):
     elapsed_ms = e0.elapsed_time(e1)
     # Per-kernel durations for the roofline: a second pass over the same
     # steps with CUDA events recorded between the two kernels (an event there
-    # also stops the update kernel from overlapping the square-sum's tail, so
-    # this pass is not the one the headline number comes from).
+    # also stops the update kernel from overlapping the square-sum's tail, and
+    # a list small enough for the single-launch step runs this pass as the two
+    # kernels, so this pass is not the one the headline number comes from).
     norm_ms = upd_ms = 0.0
     nsteps = 0
     if graph is None:
