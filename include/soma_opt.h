@@ -147,13 +147,12 @@ soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
  * finite.  Each group with at least one trainable entry in the list advances
  * its step count by one.  Enqueues two kernels on `stream` and returns without
  * waiting for them: the owned square-sum (which also derives norm and c on
- * the device) and the fused update.  A list small enough for the single-launch
- * step (soma_opt_set_single_launch) runs as one kernel instead, one thread-
- * block cluster, with the same results bit for bit, unless kernel timing is
- * on.  No device-to-host synchronisation
- * happens, except that a list the handle has not prepared yet waits for the
- * previous step's kernels before its device tables are written (see the
- * prepared-list cache below).  The group constants are fixed when the step is
+ * the device) and the fused update.  A list small enough for the
+ * single-launch step (soma_opt_set_single_launch) runs as one kernel instead,
+ * one thread-block cluster, with the same results bit for bit, unless kernel
+ * timing is on.  No device-to-host synchronisation happens, except that a
+ * list the handle has not prepared yet waits for the previous step's kernels
+ * before its device tables are written (see the prepared-list cache below).  The group constants are fixed when the step is
  * enqueued, so a capturing `stream` gets SOMA_ERR_STATE: capture
  * soma_opt_step_graph instead. */
 soma_status_t soma_opt_step(soma_opt_t opt, const soma_tensor_t *list, int64_t n,
@@ -245,8 +244,10 @@ soma_status_t soma_opt_get_norm(soma_opt_t opt, double *norm, double *clip_coef,
                                 int32_t *nonfinite, void *stream);
 
 /* Kernel timing: when enabled, each step records CUDA events around its two
- * kernels on the step's stream.  read_timing waits for them and returns the
- * summed kernel times (ms) and the number of steps since the last read. */
+ * kernels on the step's stream (a timed step always runs as the two kernels,
+ * also for a list that would otherwise take the single-launch step).
+ * read_timing waits for them and returns the summed kernel times (ms) and the
+ * number of steps since the last read. */
 soma_status_t soma_opt_set_timing(soma_opt_t opt, int32_t enable);
 soma_status_t soma_opt_read_timing(soma_opt_t opt, double *norm_ms, double *update_ms,
                                    int64_t *steps);
@@ -289,20 +290,20 @@ soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t 
                                   int32_t update_ctas_per_sm, int32_t norm_ctas_per_sm);
 
 /* Single-launch step for small lists.  For a list of at most max_elements
- * trainable elements, a regular step is one kernel: one thread-block cluster
- * (16 CTAs where the device can run such a cluster, else 8, 4 or 2) whose CTAs
- * square-sum their share of the norm chunks, meet at the hardware cluster
- * barrier, each add all chunk sums in the fixed order of the two-kernel path
- * (so each derives the same c), and update their share of the list.  The
- * chain of two dependent kernels costs more than the work of such a list.
- * Such lists are cut into about one chunk per CTA in both tables (unless
- * soma_opt_set_tuning fixed the chunk sizes), and the two-kernel path (timed
- * steps, the multi-rank step) uses the same tables, so every path gives the
- * same bits.  max_elements: -1 = automatic
- * (4096 per CTA of the cluster, one 8-element vector per thread: 65536 with
- * 16 CTAs; larger lists ran faster as two kernels on GB300), 0 = never.  Drops the
- * prepared lists like soma_opt_set_tuning, and like it fails with
- * SOMA_ERR_STATE on a handle that ran a graph-capturable step. */
+ * trainable elements, a regular or graph-capturable step is one kernel: one
+ * thread-block cluster (16 CTAs where the device can run such a cluster, else
+ * 8, 4 or 2) whose CTAs square-sum their share of the norm chunks, meet at
+ * the hardware cluster barrier, each add all chunk sums in the fixed order of
+ * the two-kernel path (so each derives the same c), and update their share of
+ * the list.  The chain of two dependent kernels costs more than the work of
+ * such a list.  Such lists are cut into about one chunk per CTA in both
+ * tables (unless soma_opt_set_tuning fixed the chunk sizes), and the
+ * two-kernel path (timed steps, the multi-rank step) uses the same tables, so
+ * every path gives the same bits.  max_elements: -1 = automatic (4096 per CTA
+ * of the cluster, one 8-element vector per thread: 65536 with 16 CTAs; larger
+ * lists ran faster as two kernels on GB300), 0 = never.  Drops the prepared
+ * lists like soma_opt_set_tuning, and like it fails with SOMA_ERR_STATE on a
+ * handle that ran a graph-capturable step. */
 soma_status_t soma_opt_set_single_launch(soma_opt_t opt, int64_t max_elements);
 
 /* Text of a status code (static storage). */
