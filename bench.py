@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--tuning", default="",
                     help="update_chunk,norm_chunk,update_ctas_per_sm,norm_ctas_per_sm (0 = default)")
+    ap.add_argument("--single-launch", type=int, default=-1,
+                    help="lists with at most this many trainable elements run as one cluster launch "
+                         "(-1 = automatic, 0 = always the two kernels)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step (soma_opt_step_graph) in a CUDA graph and time its replays")
     ap.add_argument("--master", action="store_true",
@@ -475,6 +478,8 @@ def run_ours(args):
         opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
     if args.tuning:
         opt.set_tuning(*(int(x) for x in args.tuning.split(",")))
+    if args.single_launch != -1:
+        opt.set_single_launch(args.single_launch)
     tl = TensorList(p, g, m, v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
                     owned=[t.owned for t in w.tensors], params_lowp=fb.plow)
     stream = torch.cuda.current_stream(device)
