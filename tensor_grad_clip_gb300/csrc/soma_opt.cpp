@@ -357,8 +357,9 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
     // cluster CTA, so each CTA's share is one pass of its threads.
     const int64_t limit = o->single_limit >= 0 ? o->single_limit : (int64_t)o->single_ctas * kSinglePerCta;
     const bool single = o->single_ctas > 0 && trainable_total <= limit;
-    auto per_cta = [&](int64_t total) {
-        return std::max<int64_t>(64, (total + o->single_ctas - 1) / std::max(o->single_ctas, 1) + 63) / 64 * 64;
+    auto per_cta = [&](int64_t total) {  // ceil(total / CTAs), rounded up to a multiple of 64, at least 64
+        const int64_t k = std::max(o->single_ctas, 1);
+        return std::max<int64_t>(64, ((total + k - 1) / k + 63) / 64 * 64);
     };
     TableBuilder upd(o->update_chunk == 0 && single ? per_cta(trainable_total)
                                                     : chunk_size(o->update_chunk, kDefaultUpdateChunk,
