@@ -282,7 +282,9 @@ soma_status_t soma_opt_get_cache_stats(soma_opt_t opt, int64_t *builds, int64_t 
 
 /* Tuning knobs for benchmarks: elements per update chunk and per norm chunk
  * (rounded to a multiple of 64; 0 = automatic: 16 Ki / 112 Ki elements, less
- * for lists too small to give every SM four chunks, never below 1 Ki) and,
+ * for lists too small to give every SM four chunks, never below 1 Ki; norm
+ * chunks of 320 Ki with a shrinking tail for lists whose owned tensors
+ * average at least 320 Ki elements) and,
  * per kernel, resident CTAs per SM for a persistent grid (0 = one CTA per
  * chunk).  Results do not depend on the grid, only on the chunk sizes.  Takes
  * effect at the next list (re)build. */
