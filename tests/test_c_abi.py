@@ -25,6 +25,20 @@ def test_c99_program_uses_the_library(tmp_path):
     assert "c abi ok" in out.stdout
 
 
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+def test_header_links_from_cpp(tmp_path):
+    # the same program built as C++17: the header's extern "C" block gives the
+    # library's unmangled names
+    lib = build.build()
+    exe = tmp_path / "abi_check_cpp"
+    subprocess.run(["g++", "-std=c++17", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    "-x", "c++", os.path.join(HERE, "c_abi", "abi_check.c"), "-x", "none", "-o", str(exe), lib,
+                    "-Wl,-rpath," + os.path.dirname(lib)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "c abi ok" in out.stdout
+
+
 @pytest.mark.gpu
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
 def test_c99_program_runs_a_step(tmp_path):
