@@ -52,6 +52,18 @@ int main(void) {
     CHECK(soma_opt_get_cache_stats(opt, &builds, &reuses, &entries) == SOMA_OK);
     CHECK(builds == 0 && reuses == 0 && entries == 0);
 
+    /* host-side knobs: tuning and the single-launch limit */
+    CHECK(soma_opt_set_tuning(opt, 4096, 8192, 0, 0) == SOMA_OK);
+    CHECK(soma_opt_set_tuning(opt, 10, 0, 0, 0) == SOMA_ERR_INVALID_ARG);
+    CHECK(soma_opt_set_single_launch(opt, 0) == SOMA_OK);
+    CHECK(soma_opt_set_single_launch(opt, -1) == SOMA_OK);
+    CHECK(soma_opt_set_single_launch(opt, -2) == SOMA_ERR_INVALID_ARG);
+    soma_plan_t plan;
+    memset(&plan, 0xff, sizeof plan);
+    CHECK(soma_opt_get_plan(opt, &plan) == SOMA_OK);
+    CHECK(plan.launches_per_step == 0 && plan.single_launch_ctas == 0); /* no step yet */
+    CHECK(sizeof(soma_plan_t) == 72);
+
     soma_opt_destroy(opt);
     CHECK(soma_opt_set_lr(opt, 0, 1e-3) == SOMA_ERR_STATE); /* a destroyed handle is refused */
     puts("c abi ok");
