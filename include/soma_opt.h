@@ -70,7 +70,7 @@ typedef int32_t soma_status_t;
 #define SOMA_DTYPE_F16   2  /* IEEE binary16 */
 
 #define SOMA_MAX_GROUPS  64
-#define SOMA_ABI_VERSION 4
+#define SOMA_ABI_VERSION 5
 
 typedef struct soma_opt soma_opt;
 typedef soma_opt *soma_opt_t;
@@ -113,19 +113,32 @@ typedef struct {
 } soma_tensor_t;
 
 /* Create a handle bound to CUDA device `device`.  Makes no CUDA call: device
- * memory is allocated on the first step.  *out is set to NULL on failure. */
+ * memory is allocated on the first step.  *out is set to NULL on failure.
+ * The handle stands for the optimizer object of the unfused step that the
+ * veRL write-up runs after clip_grad_norm_ ("veRL Training Process", 4.2 PPO
+ * Update): it holds the group settings and step counts, while the weights
+ * and moments it updates stay in the caller's buffers (see "Ownership of
+ * memory" above). */
 soma_status_t soma_opt_create(soma_opt_t *out, int32_t device);
 
 /* Add a parameter group with torch.optim.AdamW's hyperparameters
  * (lr >= 0, 0 <= beta1, beta2 < 1, eps > 0, weight_decay >= 0, all finite).
- * Its step count starts at 0.  Writes the new id (0, 1, ...) to *group_id. */
+ * Its step count starts at 0.  Writes the new id (0, 1, ...) to *group_id.
+ * Groups exist because the fused step must keep each parameter group's
+ * configured behaviour (SomaSpeed page, second optimizer paragraph), as
+ * RLinf's FP32MasterAdamW keeps the groups and settings of the optimizer it
+ * replaces (RLinf page, "Retaining Low-Precision Gradients"). */
 soma_status_t soma_opt_add_group(soma_opt_t opt, double lr, double beta1, double beta2,
                                  double eps, double weight_decay, int32_t *group_id);
 
-/* Change a group's lr (learning-rate schedules); applies to the next step. */
+/* Change a group's lr; applies to the next step.  This is how a
+ * learning-rate schedule reaches the fused step, whose schedules keep their
+ * configured behaviour (SomaSpeed page, second optimizer paragraph). */
 soma_status_t soma_opt_set_lr(soma_opt_t opt, int32_t group, double lr);
 
-/* Read or replace all hyperparameters of a group (same ranges as add_group). */
+/* Read or replace all hyperparameters of a group (same ranges as add_group):
+ * the group settings that the fused step preserves (SomaSpeed page, second
+ * optimizer paragraph; RLinf page, "Retaining Low-Precision Gradients"). */
 soma_status_t soma_opt_get_group(soma_opt_t opt, int32_t group, double *lr, double *beta1,
                                  double *beta2, double *eps, double *weight_decay);
 soma_status_t soma_opt_set_group(soma_opt_t opt, int32_t group, double lr, double beta1,
@@ -134,11 +147,19 @@ soma_status_t soma_opt_set_group(soma_opt_t opt, int32_t group, double lr, doubl
 /* A group's own effective-batch divisor: its gradients are normalized by it
  * (in the norm and in the update) instead of the step's grad_divisor, e.g.
  * for parameters accumulated over a different number of micro-batches.
- * divisor > 0 and finite, or 0 to use the step's divisor (the default). */
+ * divisor > 0 and finite, or 0 to use the step's divisor (the default).
+ * The normalization is the first thing the SomaSpeed page's step does to a
+ * gradient (its first optimizer paragraph); the veRL write-up divides the
+ * loss by the number of accumulated micro-batches (4.2 PPO Update), and
+ * groups accumulated over different counts divide by different numbers. */
 soma_status_t soma_opt_set_group_divisor(soma_opt_t opt, int32_t group, double divisor);
 soma_status_t soma_opt_get_group_divisor(soma_opt_t opt, int32_t group, double *divisor);
 
-/* Step count of a group (checkpoint and resume).  set: t >= 0. */
+/* Step count of a group (checkpoint and resume).  set: t >= 0.  AdamW's
+ * bias corrections depend on it, so a resumed run must restore it to keep
+ * the group's configured behaviour (SomaSpeed page, second optimizer
+ * paragraph); the veRL write-up saves checkpoints every 20 training steps
+ * ("Complete Training Loop", step 7, Checkpoint Saving). */
 soma_status_t soma_opt_get_group_step(soma_opt_t opt, int32_t group, int64_t *t);
 soma_status_t soma_opt_set_group_step(soma_opt_t opt, int32_t group, int64_t t);
 
@@ -234,7 +255,10 @@ soma_status_t soma_opt_step_from_sumsq(soma_opt_t opt, const soma_tensor_t *list
                                        double grad_divisor, double max_norm,
                                        const double *rank_sumsq, int32_t nranks, void *stream);
 
-/* Norm and clip coefficient of the last step (fp64), and the number of steps
+/* Norm and clip coefficient of the last step (fp64): the total norm that
+ * torch.nn.utils.clip_grad_norm_ returns in the unfused step of the veRL
+ * write-up ("veRL Training Process", 4.2 PPO Update), read here from device
+ * memory after the fused step.  Also the number of steps
  * since the previous soma_opt_get_norm on this handle whose norm was not
  * finite (so at least 1 if the last step's was not; a loop that reads the norm
  * only every few steps still learns of a non-finite one in between).  Any
@@ -264,6 +288,29 @@ typedef struct {
     int32_t single_launch_ctas;
 } soma_plan_t;
 soma_status_t soma_opt_get_plan(soma_opt_t opt, soma_plan_t *plan);
+
+/* Segment table of the last step's list, for tests and debugging.  A table
+ * cuts the list's tensors into segments (a contiguous element range of one
+ * tensor) and groups them into chunks of about the same size; one CTA
+ * processes one chunk.  The update table covers every trainable element, the
+ * norm table the trainable, owned ones (the work that the SomaSpeed page
+ * batches across tensors, its second optimizer paragraph).
+ *   grad   address of the segment's first gradient element, so that
+ *          (grad - tensor's grad) / element size is its offset in the tensor
+ *   chunk  index of the chunk that holds the segment (chunks in table order)
+ *   len    elements; head: elements before the 8-element vector body;
+ *   nvec   vectors in the body; group: the entry's group
+ * which: 0 = update table, 1 = norm table.  Writes the table's segment
+ * count to *count and its first min(cap, count) segments to out (out may be
+ * NULL when cap is 0).  Waits for the handle's last step; SOMA_ERR_STATE
+ * before the first step. */
+typedef struct {
+    const void *grad;
+    int64_t chunk;
+    int32_t len, head, nvec, group;
+} soma_segment_t;
+soma_status_t soma_opt_get_segments(soma_opt_t opt, int32_t which, soma_segment_t *out, int64_t cap,
+                                    int64_t *count);
 
 /* Prepared-list cache.  A handle keeps the device tables of the last
  * SOMA_PLAN_CACHE distinct lists it stepped (lists compared entry by entry,
@@ -319,7 +366,10 @@ const char *soma_opt_last_error(soma_opt_t opt);
 int32_t soma_abi_version(void);
 
 /* Wait for the handle's outstanding work, free its device and host memory
- * and the handle.  NULL is ignored. */
+ * and the handle.  NULL is ignored.  Only what the library allocated is freed
+ * ("Ownership of memory" above): the caller's weights, gradients and moments,
+ * the state of the unfused AdamW this step replaces (veRL write-up, 4.2 PPO
+ * Update), are left as they are. */
 void soma_opt_destroy(soma_opt_t opt);
 
 /* ---- norm without allocation ---------------------------------------------
@@ -329,24 +379,33 @@ void soma_opt_destroy(soma_opt_t opt);
  * latency-critical loop where cudaMalloc/cudaFree, which can synchronise the
  * device, are not allowed.
  *
- * Computes, on `stream`, the same norm and clip coefficient as the first
- * kernel of soma_opt_step (norm over trainable, owned entries of `list`,
+ * Computes, on `stream`, the norm and clip coefficient that the first kernel
+ * of soma_opt_step computes (norm over trainable, owned entries of `list`,
  * c = min(1, max_norm / (norm + 1e-6))) and writes them as two doubles
- * {norm, c} to `out` (device memory, 8-byte aligned, caller-owned).  It
- * updates nothing and needs no handle; only the entries' grad, grad_dtype,
- * numel, trainable and owned fields are read.
+ * {norm, c} to `out` (device memory, 8-byte aligned, caller-owned).  Its
+ * chunks are larger than the step's, so its partial sums are added in a
+ * different grouping: the two norms agree within 1e-5 relative, not bit for
+ * bit.  It updates nothing and needs no handle; only the entries' grad,
+ * grad_dtype, numel, trainable and owned fields are read.
  *
  * Scratch: a fixed array of SOMA_NOALLOC_SCRATCH_BYTES (4 MiB) in the
- * library's device image, held by every GPU that loads the library until the
- * process exits.  No cudaMalloc, cudaFree or other allocating call is made.
- * A list whose tables and partial sums do not fit returns SOMA_ERR_LIMIT
- * before anything is enqueued (with chunks of at least 32 Ki elements, about
- * 20 000 owned entries fit, of any total size).
+ * library's device image.  The CUDA runtime loads that image lazily, so the
+ * array takes its 4 MiB of device memory on the first call on each device and
+ * keeps it until the process exits: make that first call while 4 MiB are
+ * still free, before the caller's own allocator reserves the device heap.  No
+ * cudaMalloc, cudaFree or other allocating call is made.  A list whose tables
+ * and partial sums do not fit returns SOMA_ERR_LIMIT before anything is
+ * enqueued.  Each owned entry takes at least one 64-byte segment, and a list
+ * is cut into at most about 32 768 chunks of at least 32 Ki elements, so at
+ * least 26 000 owned entries fit whatever their sizes (about 64 000 when they
+ * are small enough to share chunks).
  *
- * The call returns once the tables have been copied into the array (it waits
- * on `stream` for that copy); the kernel and the copy to `out` stay queued.
- * The first call on a device, with that device made current, looks up the
- * array's device address and keeps it; make that first call before any stream
+ * Blocking: each call copies the tables from a host buffer that the next call
+ * rewrites, and waits for `stream` after that copy, so it returns only once
+ * all work enqueued earlier on `stream` (the caller's backward pass, say) has
+ * finished; the kernel and the copy to `out` then stay queued.  The first
+ * call on a device, with that device made current, also looks up the array's
+ * device address and keeps it; make that first call before any stream
  * capture.  Every call shares the array and overwrites what the previous call
  * left there (it clears the result block each time).  Calls that overlap on
  * the GPU -- on unordered streams, or from several host threads -- race on

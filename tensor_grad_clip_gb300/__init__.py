@@ -282,6 +282,20 @@ class SomaOpt:
         self._check(_abi.soma_opt_get_plan(self._h, ctypes.byref(p)))
         return {name: getattr(p, name) for name, _ in soma_plan_t._fields_}
 
+    def segments(self, which: str = "update") -> dict:
+        """Segment table of the last step's list ("update" or "norm") as
+        numpy arrays: grad (address of the first gradient element), chunk,
+        len, head, nvec, group.  Waits for the last step."""
+        import numpy as np
+        code = {"update": 0, "norm": 1}[which]
+        n = ctypes.c_int64()
+        self._check(_abi.soma_opt_get_segments(self._h, code, None, 0, ctypes.byref(n)))
+        arr = (_abi.soma_segment_t * max(1, n.value))()
+        self._check(_abi.soma_opt_get_segments(self._h, code, arr, n.value, ctypes.byref(n)))
+        raw = np.frombuffer(arr, dtype=np.dtype([("grad", "<u8"), ("chunk", "<i8"), ("len", "<i4"), ("head", "<i4"),
+                                                 ("nvec", "<i4"), ("group", "<i4")]))[:n.value]
+        return {name: raw[name].copy() for name in raw.dtype.names}
+
     def cache_stats(self) -> dict:
         """Prepared-list cache: table builds, steps that reused a prepared
         list, lists held now."""

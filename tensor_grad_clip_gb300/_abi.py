@@ -24,7 +24,7 @@ SOMA_DTYPE_F32 = 0
 SOMA_DTYPE_BF16 = 1
 SOMA_DTYPE_F16 = 2
 SOMA_MAX_GROUPS = 64
-SOMA_ABI_VERSION = 4
+SOMA_ABI_VERSION = 5
 SOMA_MAX_RANKS = 65536
 SOMA_PLAN_CACHE = 4
 
@@ -68,6 +68,14 @@ class soma_plan_t(ctypes.Structure):
     ]
 
 
+class soma_segment_t(ctypes.Structure):
+    _fields_ = [("grad", ctypes.c_void_p), ("chunk", ctypes.c_int64), ("len", ctypes.c_int32),
+                ("head", ctypes.c_int32), ("nvec", ctypes.c_int32), ("group", ctypes.c_int32)]
+
+
+assert ctypes.sizeof(soma_segment_t) == 32
+
+
 class soma_device_group_t(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64),
@@ -101,6 +109,7 @@ SIGNATURES = {
     "soma_opt_read_timing": (soma_status_t, [soma_opt_t, _DP, _DP, _I64P]),
     "soma_opt_get_plan": (soma_status_t, [soma_opt_t, ctypes.POINTER(soma_plan_t)]),
     "soma_opt_get_cache_stats": (soma_status_t, [soma_opt_t, _I64P, _I64P, _I32P]),
+    "soma_opt_get_segments": (soma_status_t, [soma_opt_t, _I32, ctypes.POINTER(soma_segment_t), _I64, _I64P]),
     "soma_opt_set_tuning": (soma_status_t, [soma_opt_t, _I32, _I32, _I32, _I32]),
     "soma_opt_set_single_launch": (soma_status_t, [soma_opt_t, _I64]),
     "soma_status_string": (ctypes.c_char_p, [soma_status_t]),

@@ -9,12 +9,18 @@
 // entry point runs the square-sum kernel with all of its scratch (the
 // arrival ticket and result, the per-chunk partial sums and the chunk /
 // segment tables) placed in one file-scope __device__ array of fixed size.
-// Every GPU that loads the library holds that array until the process exits.
+// The runtime loads this file's device image lazily: the array takes its
+// device memory on the first call on a device (when cudaGetSymbolAddress
+// loads the image) and keeps it until the process exits.
 //
 // Set-up: the first call on a device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress (in host code the array's
 // name is only a host-side stand-in, not a device address) and caches it.
 // Make that first call before any stream capture.
+//
+// Each call waits for its stream after copying the tables (see the copy
+// below), so it returns only once everything enqueued earlier on that stream
+// has finished.
 //
 // All calls share the one array, which keeps the contents of the last call:
 // every call rewrites the tables and clears the result/ticket block before
@@ -52,10 +58,12 @@ void* g_dev_scratch[kMaxDevices];              // per device: address of the arr
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Counts (segs == nullptr) or writes the norm table: the
-// trainable, owned entries cut into segments, grouped into chunks of about
-// `chunk` elements and at most kMaxSegsPerChunk segments each.  The vector
-// head is the number of leading elements before the gradient is 16-byte
-// aligned.
+// trainable, owned entries cut into segments by the step's own cutting rule
+// (soma::segment_cut), grouped into chunks of about `chunk` elements and at
+// most kMaxSegsPerChunk segments each.  The vector head is the number of
+// leading elements before the gradient is 16-byte aligned.  The step's
+// table builder keeps its segments in a growing array; this one writes into
+// the fixed staging buffer and allocates nothing.
 void norm_table(const soma_tensor_t* list, int64_t n, int64_t chunk, soma::Seg* segs, int32_t* begin,
                 int64_t* nseg_out, int64_t* nchunk_out) {
     int64_t nseg = 0, nchunk = 0, cur_elems = 0;
@@ -76,23 +84,12 @@ void norm_table(const soma_tensor_t* list, int64_t n, int64_t chunk, soma::Seg* 
                 cur_elems = 0;
                 cur_segs = 0;
             }
-            int64_t cut = off + std::min(t.numel - off, chunk - cur_elems);
-            if (h >= 0 && cut < t.numel && cut > h) {
-                cut = h + (cut - h + soma::kVec - 1) / soma::kVec * soma::kVec;
-                if (cut > t.numel) cut = t.numel;
-            }
+            const int64_t cut = soma::segment_cut(off, t.numel, chunk - cur_elems, h);
             const int64_t len = cut - off;
             if (segs) {
                 soma::Seg s{};
                 s.g = static_cast<const char*>(t.grad) + off * gsz;
-                s.len = (int32_t)len;
-                if (h < 0) {
-                    s.head = (int32_t)len;
-                    s.nvec = 0;
-                } else {
-                    s.head = off < h ? (int32_t)std::min<int64_t>(h - off, len) : 0;
-                    s.nvec = (int32_t)((len - s.head) / soma::kVec);
-                }
+                soma::segment_body(off, len, h, s);
                 s.gdtype = t.grad_dtype;
                 segs[nseg] = s;
             }

@@ -186,6 +186,33 @@ struct UpdateArgs {
     const float* gscale;          // group divisors: c / d of each group, written by the norm side
 };
 
+// Host-side cutting rule shared by every table builder.  A segment that
+// starts at element `off` of an n-element tensor with vector head h (-1 =
+// no vector body) and may take up to `room` elements ends at the returned
+// element: a cut inside the tensor is moved up to the vector grid h + 8j, so
+// that only a tensor's first and last segments have scalar elements outside
+// their vector bodies.
+inline int64_t segment_cut(int64_t off, int64_t n, int64_t room, int h) {
+    int64_t cut = off + (n - off < room ? n - off : room);
+    if (h >= 0 && cut < n && cut > h) {
+        cut = h + (cut - h + kVec - 1) / kVec * kVec;
+        if (cut > n) cut = n;
+    }
+    return cut;
+}
+
+// head and nvec of the segment [off, off + len) of a tensor with vector head h.
+inline void segment_body(int64_t off, int64_t len, int h, Seg& s) {
+    s.len = (int32_t)len;
+    if (h < 0) {
+        s.head = (int32_t)len;
+        s.nvec = 0;
+    } else {
+        s.head = off < h ? (int32_t)(h - off < len ? h - off : len) : 0;
+        s.nvec = (int32_t)((len - s.head) / kVec);
+    }
+}
+
 constexpr int kNormBlock = 512;
 constexpr int kUpdateBlock = 256;
 

@@ -9,6 +9,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <array>
 #include <cmath>
 #include <cstdarg>
@@ -262,11 +263,7 @@ struct TableBuilder {
                 close();
             if (cur_segs == 0) cur_target = target();
             cur_group = t.group;
-            int64_t cut = off + std::min(n - off, cur_target - cur_elems);
-            if (h >= 0 && cut < n && cut > h) {  // cut on the vector grid
-                cut = h + (cut - h + soma::kVec - 1) / soma::kVec * soma::kVec;
-                if (cut > n) cut = n;
-            }
+            const int64_t cut = soma::segment_cut(off, n, cur_target - cur_elems, h);
             const int64_t len = cut - off;
             soma::Seg s{};
             s.p = with_state ? t.param + off : nullptr;
@@ -275,14 +272,7 @@ struct TableBuilder {
             s.g = static_cast<const char*>(t.grad) + off * gsz;
             s.plow = (with_state && t.param_lowp) ? static_cast<char*>(t.param_lowp) + off * 2 : nullptr;
             s.lowdt = (with_state && t.param_lowp) ? t.lowp_dtype : 0;
-            s.len = (int32_t)len;
-            if (h < 0) {
-                s.head = (int32_t)len;
-                s.nvec = 0;
-            } else {
-                s.head = off < h ? (int32_t)std::min<int64_t>(h - off, len) : 0;
-                s.nvec = (int32_t)((len - s.head) / soma::kVec);
-            }
+            soma::segment_body(off, len, h, s);
             s.group = (uint16_t)t.group;
             s.gdtype = t.grad_dtype;
             segs.push_back(s);
@@ -1167,6 +1157,37 @@ soma_status_t soma_opt_get_plan(soma_opt_t h, soma_plan_t* plan) {
     if (!o) return SOMA_ERR_STATE;
     if (!plan) return o->fail(SOMA_ERR_INVALID_ARG, "plan is NULL");
     *plan = o->plan;
+    return SOMA_OK;
+}
+
+soma_status_t soma_opt_get_segments(soma_opt_t h, int32_t which, soma_segment_t* out, int64_t cap,
+                                    int64_t* count) {
+    soma_opt* o = live_handle(h);
+    if (!o) return SOMA_ERR_STATE;
+    if (which != 0 && which != 1) return o->fail(SOMA_ERR_INVALID_ARG, "which must be 0 (update) or 1 (norm)");
+    if (!count || cap < 0 || (cap > 0 && !out)) return o->fail(SOMA_ERR_INVALID_ARG, "bad output arguments");
+    if (o->active < 0) return o->fail(SOMA_ERR_STATE, "no step has run on this handle yet");
+    const soma::Table& t = which == 0 ? o->upd_tab : o->norm_tab;
+    DeviceGuard dg(o->device);
+    if (dg.status != cudaSuccess) return o->cuda_fail(dg.status, "cudaSetDevice");
+    soma_status_t st = wait_idle(o);  // the tables' upload is ordered before the last step
+    if (st != SOMA_OK) return st;
+    std::vector<int32_t> begin((size_t)t.nchunks + 1);
+    cudaError_t e = cudaMemcpy(begin.data(), t.chunk_begin, begin.size() * sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return o->cuda_fail(e, "cudaMemcpy(chunk table)");
+    const int64_t nseg = begin.back();
+    *count = nseg;
+    const int64_t take = std::min<int64_t>(cap, nseg);
+    if (take == 0) return SOMA_OK;
+    std::vector<soma::Seg> segs((size_t)take);
+    if ((e = cudaMemcpy(segs.data(), t.segs, segs.size() * sizeof(soma::Seg), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return o->cuda_fail(e, "cudaMemcpy(segment table)");
+    int64_t c = 0;
+    for (int64_t i = 0; i < take; ++i) {
+        while (c + 1 < (int64_t)begin.size() && begin[(size_t)c + 1] <= i) ++c;
+        const soma::Seg& sg = segs[(size_t)i];
+        out[i] = soma_segment_t{sg.g, c, sg.len, sg.head, sg.nvec, (int32_t)sg.group};
+    }
     return SOMA_OK;
 }
 
