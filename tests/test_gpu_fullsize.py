@@ -1,20 +1,28 @@
 """Parity at full size, in the layout and launch configuration bench.py times.
 
-The 20 000-tensor list (104 M) is compared element by element after each of
-3 chained steps.  For the action-expert (302 M), 7B shard-view (6.48 G) and
-flat (1.5 G) lists, over 10 chained steps:
+Every element, after each chained step:
 
-* the norm is the oracle's own fp64 sum over every owned gradient, taken
-  in pieces of at most 2^26 elements on a thread pool and added in list
-  order;
-* the update is checked on a seeded sample of elements per tensor: the first
-  and last 32 and 128 random ones.  The oracle carries their fp64 state
-  across steps, each element depending only on its own p, m, v, g, the
-  oracle's c and the group constants;
-* gradients are bit-unchanged, and the sentinel gaps between tensors are
-  intact.
+* the action-expert list (302 M parameters) and the flat list (1.5 G + 256):
+  10 steps, the fp64 oracle state of every element kept on the host
+  (7.2 GB and 36 GB) and updated by the oracle's own per-tensor function on
+  slices of 1 Mi elements over a thread pool;
+* the 20 000-tensor list (104 M): 3 steps through the oracle's whole step.
 
-A single tensor of more than 2^31 elements covers 64-bit offsets.
+The 7B shard view (6.48 G) would need 155 GB of fp64 state, so it is checked
+over 10 steps on:
+
+* every element of its first and last block (16 tensors, both groups, owned
+  and replicated ones: 404 M elements);
+* a 64-element window around the start of every segment of both tables
+  (soma_opt_get_segments), so that every chunk boundary, every cut of a
+  large tensor and every tensor's first and last elements are seen
+  (about 25 M elements);
+* 128 random elements per tensor.
+
+For every list the norm is the oracle's fp64 sum over every owned gradient
+(in pieces of at most 2^26 elements, added in list order), the gradients are
+bit-unchanged and the sentinel gaps between tensors are intact.  A single
+tensor of more than 2^31 elements covers 64-bit offsets.
 """
 import math
 from concurrent.futures import ThreadPoolExecutor
@@ -25,10 +33,13 @@ import torch
 
 import oracle
 import workloads as W
-from parity_harness import NORM_RTOL, assert_close
+from parity_harness import ATOL, NORM_RTOL, RTOL, assert_close
 from tensor_grad_clip_gb300 import SomaOpt, TensorList, build
 
 pytestmark = pytest.mark.gpu
+
+SLICE = 1 << 20
+POOL = 16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -37,32 +48,69 @@ def _built():
     oracle.lib()
 
 
-def oracle_norm(w, fb, divisor, pool):
+def oracle_norm(w, host_g, divisor, pool):
     """sqrt of the oracle's sum of (g/d)^2 over owned tensors; large tensors
     are summed in pieces of 2^26 elements, pieces added in list order."""
     piece = 1 << 26
     tasks = [(k, a) for k, t in enumerate(w.tensors) if t.trainable and t.owned
              for a in range(0, t.numel, piece)]
-
-    def one(task):
-        k, a = task
-        return oracle.tensor_sqsum(fb.g[k][a:a + piece].cpu(), divisor)
-
     total = 0.0
-    for x in pool.map(one, tasks):
+    for x in pool.map(lambda ka: oracle.tensor_sqsum(host_g[ka[0]][ka[1]:ka[1] + piece], divisor), tasks):
         total += x
     return math.sqrt(total)
 
 
-def sample_indices(numel, seed, k):
-    rng = np.random.default_rng(seed * 1000 + k)
-    head = np.arange(min(32, numel))
-    tail = np.arange(max(0, numel - 32), numel)
-    rand = rng.integers(0, numel, size=min(128, numel))
-    return np.unique(np.concatenate([head, tail, rand]))
+def _bad(got, ref):
+    """Elements outside |got - ref| <= RTOL |ref| + ATOL (NaN counts as out)."""
+    got = got.astype(np.float64)
+    err = np.abs(got - ref)
+    bound = np.abs(ref)
+    bound *= RTOL
+    bound += ATOL
+    return ~(err <= bound)
 
 
-def run_full(w, steps, extra_idx=None, graph=False):
+def _segment_starts(opt, fb, w):
+    """Per tensor, the element offsets at which a segment of either table
+    starts (from the segment tables the last step ran).  Also checks that the
+    segments tile each table's tensors exactly: every segment inside its
+    tensor, consecutive within it, covering it once."""
+    esize = fb.G.element_size()
+    base = fb.G.data_ptr()
+    offs = np.asarray(fb.offsets, dtype=np.int64)
+    numel = np.asarray([t.numel for t in w.tensors], dtype=np.int64)
+    starts = [[] for _ in w.tensors]
+    for which in ("update", "norm"):
+        seg = opt.segments(which)
+        e = (seg["grad"].astype(np.int64) - base) // esize
+        k = np.searchsorted(offs, e, side="right") - 1
+        off = e - offs[k]
+        assert np.all((off >= 0) & (off + seg["len"] <= numel[k])), which
+        covered = np.bincount(k, weights=seg["len"], minlength=len(w.tensors)).astype(np.int64)
+        want = np.asarray([t.numel if t.trainable and (which == "update" or t.owned) else 0
+                           for t in w.tensors], dtype=np.int64)
+        assert np.array_equal(covered, want), which
+        for kk in np.unique(k):
+            sk = off[k == kk]
+            assert np.all(np.diff(sk) > 0) and sk[0] == 0, which  # in order, from the tensor's start
+            starts[kk].append(sk)
+    return [np.unique(np.concatenate(s)) if s else np.zeros(0, np.int64) for s in starts]
+
+
+def _windows(starts, numel, half=32):
+    if numel == 0 or starts.size == 0:
+        return np.zeros(0, np.int64)
+    ix = (starts[:, None] + np.arange(-half, half)[None, :]).reshape(-1)
+    return np.unique(ix[(ix >= 0) & (ix < numel)])
+
+
+def run_full(w, steps, select=None, graph=False, extra_idx=None):
+    """Chained steps of `w` at full size against the fp64 oracle.
+
+    select(opt, fb) -> per tensor None (every element) or an index array,
+    called once after the first step (the segment tables exist then); None
+    checks every element of every tensor.  extra_idx is added to every
+    sampled tensor."""
     dev = torch.device("cuda", 0)
     fb = W.FlatBuffers(w, dev, grad_step=1)
     opt = SomaOpt(0)
@@ -70,26 +118,22 @@ def run_full(w, steps, extra_idx=None, graph=False):
         opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
     tl = TensorList(fb.p, fb.g, fb.m, fb.v, groups=[t.group for t in w.tensors],
                     trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
-    idx, state = [], []
-    for k, t in enumerate(w.tensors):
-        ix = sample_indices(t.numel, w.seed, k)
-        if extra_idx is not None:
-            ix = np.unique(np.concatenate([ix, extra_idx]))
-        ix_t = torch.from_numpy(ix).to(dev)
-        idx.append(ix_t)
-        p0 = fb.p[k][ix_t].double().cpu().numpy()
-        state.append([p0.copy(), np.zeros_like(p0), np.zeros_like(p0)])
-    pool = ThreadPoolExecutor(16)
+    p0 = [x.cpu() for x in fb.p]  # initial weights: fp32, converted to fp64 per checked element
+    pool = ThreadPoolExecutor(POOL)
     stream = torch.cuda.Stream() if graph else None
     cuda_graph = torch.cuda.CUDAGraph() if graph else None
+    gbits = torch.int16 if fb.grad_dtype == torch.bfloat16 else torch.int32
+    idx = idx_t = state = host = None
+    checked = 0
     for s in range(1, steps + 1):
         if s > 1:
             fb.load_grads(s)
         lrs = w.group_lrs(s)
         for q, lr in enumerate(lrs):
             opt.set_lr(q, lr)
-        gbits = torch.int16 if fb.grad_dtype == torch.bfloat16 else torch.int32
         g_before = fb.G.view(gbits).clone()
+        # every gradient of this step on the host, for the norm and the update
+        host_g = [x.cpu() for x in fb.g]
         if graph:  # captured once, replayed with the lr pushed each step
             stream.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(stream):
@@ -105,7 +149,7 @@ def run_full(w, steps, extra_idx=None, graph=False):
         else:
             opt.step(tl, w.grad_divisor, w.max_norm)
             norm, coef, nonfinite = opt.get_norm()
-        rn = oracle_norm(w, fb, w.grad_divisor, pool)
+        rn = oracle_norm(w, host_g, w.grad_divisor, pool)
         rc = oracle.clip_coef(rn, w.max_norm)
         assert not nonfinite
         assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (s, norm, rn)
@@ -114,15 +158,57 @@ def run_full(w, steps, extra_idx=None, graph=False):
             assert coef == 1.0
         assert torch.equal(fb.G.view(gbits), g_before), "gradients changed"
         del g_before
+
+        if idx is None:  # after the first step: choose the checked elements, seed their fp64 state
+            sel = select(opt, fb) if select is not None else [None] * len(w.tensors)
+            idx, idx_t, state, host = [], [], [], []
+            for k, t in enumerate(w.tensors):
+                ix = sel[k]
+                if ix is not None and extra_idx is not None:
+                    ix = np.unique(np.concatenate([ix, extra_idx[(extra_idx >= 0) & (extra_idx < t.numel)]]))
+                idx.append(ix)
+                idx_t.append(None if ix is None else torch.from_numpy(ix).to(dev))
+                n = t.numel if ix is None else ix.size
+                pk = p0[k].numpy() if ix is None else p0[k].numpy()[ix]
+                state.append([pk.astype(np.float64), np.zeros(n), np.zeros(n)])
+                host.append([torch.empty(n, dtype=torch.float32, pin_memory=True) for _ in range(3)])
+                checked += n if t.trainable else 0
+            del p0
+
+        # the oracle's update of every checked element, slice by slice
+        tasks = []
         for k, t in enumerate(w.tensors):
+            if not t.trainable:
+                continue
+            gk = host_g[k] if idx[k] is None else host_g[k][torch.from_numpy(idx[k])]
+            for src, dst in zip((fb.p[k], fb.m[k], fb.v[k]), host[k]):
+                dst.copy_(src if idx_t[k] is None else src[idx_t[k]])
+            for lo in range(0, gk.numel(), SLICE):
+                tasks.append((k, lo, min(gk.numel(), lo + SLICE), gk))
+
+        def one(task):
+            k, lo, hi, gk = task
+            t = w.tensors[k]
             q = w.groups[t.group]
-            p_s, m_s, v_s = state[k]
-            oracle.adamw_update(p_s, fb.g[k][idx[k]].cpu(), m_s, v_s, lr=lrs[t.group], beta1=q.beta1,
-                                beta2=q.beta2, eps=q.eps, weight_decay=q.weight_decay, step=s, c=rc,
-                                divisor=w.grad_divisor)
-            assert_close(f"step {s} {t.name} p", fb.p[k][idx[k]].cpu().numpy(), p_s)
-            assert_close(f"step {s} {t.name} m", fb.m[k][idx[k]].cpu().numpy(), m_s)
-            assert_close(f"step {s} {t.name} v", fb.v[k][idx[k]].cpu().numpy(), v_s)
+            p_s, m_s, v_s = (x[lo:hi] for x in state[k])
+            oracle.adamw_update(p_s, gk[lo:hi], m_s, v_s, lr=lrs[t.group], beta1=q.beta1, beta2=q.beta2, eps=q.eps,
+                                weight_decay=q.weight_decay, step=s, c=rc, divisor=w.grad_divisor)
+            out = []
+            for nm, got, ref in zip("pmv", host[k], (p_s, m_s, v_s)):
+                bad = _bad(got[lo:hi].numpy(), ref)
+                if bad.any():
+                    out.append((nm, k, lo, np.flatnonzero(bad)))
+            return out
+
+        for res in pool.map(one, tasks):
+            for nm, k, lo, where in res:
+                j = int(where[0])
+                ref = state[k]["pmv".index(nm)][lo:lo + j + 1]
+                got = host[k]["pmv".index(nm)][lo:lo + j + 1].numpy()
+                at = lo + j if idx[k] is None else int(idx[k][lo + j])
+                assert_close(f"step {s} {w.tensors[k].name} {nm} (element {at}, {where.size} bad in its slice)",
+                             got, ref)
+        del host_g
     if graph:
         opt.pull_groups(stream)
         del cuda_graph
@@ -135,13 +221,46 @@ def run_full(w, steps, extra_idx=None, graph=False):
     pool.shutdown()
     del fb
     torch.cuda.empty_cache()
-    return plan
+    return plan, checked
 
 
-@pytest.mark.parametrize("name", ["action_expert", "flat", "hsdp_shard"])
-def test_full_size_parity(name):
+def sample_indices(numel, seed, k):
+    rng = np.random.default_rng(seed * 1000 + k)
+    head = np.arange(min(32, numel))
+    tail = np.arange(max(0, numel - 32), numel)
+    rand = rng.integers(0, numel, size=min(128, numel))
+    return np.unique(np.concatenate([head, tail, rand]))
+
+
+def sampled(w):
+    return lambda opt, fb: [sample_indices(t.numel, w.seed, k) for k, t in enumerate(w.tensors)]
+
+
+@pytest.mark.parametrize("name", ["action_expert", "flat"])
+def test_full_size_every_element(name):
     w = W.FULL[name]()
-    plan = run_full(w, steps=10)
+    plan, checked = run_full(w, steps=10)
+    assert checked == w.trainable_numel
+    assert plan["trainable_numel"] == w.trainable_numel
+    assert plan["owned_numel"] == w.owned_numel
+
+
+def test_full_size_hsdp_shard_blocks_and_every_chunk_boundary():
+    w = W.FULL["hsdp_shard"]()
+    per_block = 8
+
+    def select(opt, fb):
+        starts = _segment_starts(opt, fb, w)
+        out = []
+        for k, t in enumerate(w.tensors):
+            if k < per_block or k >= len(w.tensors) - per_block:  # first and last block: every element
+                out.append(None)
+            else:
+                out.append(np.unique(np.concatenate([_windows(starts[k], t.numel),
+                                                     sample_indices(t.numel, w.seed, k)])))
+        return out
+
+    plan, checked = run_full(w, steps=10, select=select)
     assert plan["trainable_numel"] == w.trainable_numel
     assert plan["owned_numel"] == w.owned_numel
 
@@ -151,9 +270,9 @@ def test_full_size_graph_replays():
     # lr pushed each step (the flat list's cosine schedule), sampled against
     # the oracle like the regular step.
     w = W.with_steps(W.FULL["flat"](), 4)
-    run_full(w, steps=4, graph=True)
+    run_full(w, steps=4, select=sampled(w), graph=True)
     w = W.with_steps(W.FULL["action_expert"](), 3)
-    run_full(w, steps=3, graph=True)
+    run_full(w, steps=3, select=sampled(w), graph=True)
 
 
 def test_tensor_beyond_2_pow_31_elements():
@@ -162,7 +281,7 @@ def test_tensor_beyond_2_pow_31_elements():
                    groups=(W.GroupSpec(lr=1e-4, weight_decay=0.01),), grad_divisor=4.0, max_norm=1.0,
                    steps=2, grad_std=1e-3, seed=77)
     around = np.arange((1 << 31) - 20, (1 << 31) + 13)
-    run_full(w, steps=2, extra_idx=around)
+    run_full(w, steps=2, select=sampled(w), extra_idx=around)
 
 
 def test_full_size_many_small_every_element():
