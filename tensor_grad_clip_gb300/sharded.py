@@ -32,11 +32,16 @@ def owned_flags(num_tensors: int, rank: int, world: int, sharded: Sequence[bool]
 
 
 def gather_rank_sums(local: torch.Tensor, group=None) -> torch.Tensor:
-    """All ranks' one-element float64 tensors, rank r at index r."""
+    """All ranks' one-element float64 tensors, rank r at index r, on the
+    device of `local`.  A gloo group exchanges host copies (gloo moves host
+    memory; the copy to the host waits for the square-sum kernel)."""
     world = dist.get_world_size(group)
-    parts = [torch.empty_like(local) for _ in range(world)]
-    dist.all_gather(parts, local, group=group)
-    return torch.cat(parts)
+    staged = local.is_cuda and dist.get_backend(group) == "gloo"
+    src = local.cpu() if staged else local
+    parts = [torch.empty_like(src) for _ in range(world)]
+    dist.all_gather(parts, src, group=group)
+    out = torch.cat(parts)
+    return out.to(local.device, non_blocking=False) if staged else out
 
 
 class ShardedStep:

@@ -16,8 +16,9 @@ ALIGN = 64                  # elements: 256 B of fp32, 128 B of bf16
 
 
 class FlatBuffers:
-    def __init__(self, w: Workload, device, grad_step: int = 1, gap: int = ALIGN):
+    def __init__(self, w: Workload, device, grad_step: int = 1, gap: int = ALIGN, shard_rank: int = 0):
         self.w = w
+        self.shard_rank = shard_rank  # draws rank r's shards (see generate.draw_grad)
         self.device = torch.device(device)
         self.offsets = []
         cur = 0
@@ -54,7 +55,7 @@ class FlatBuffers:
             self.m.append(self.M[sl])
             self.v.append(self.V[sl])
             self.plow.append(self.PL[sl] if (self.PL is not None and t.param_lowp) else None)
-            self.p[-1].copy_(draw_param(w, k, self.device).reshape(-1))
+            self.p[-1].copy_(draw_param(w, k, self.device, shard_rank).reshape(-1))
             if self.plow[-1] is not None:
                 self.plow[-1].copy_(self.p[-1].to(self.PL.dtype))
             self.m[-1].zero_()
@@ -63,7 +64,7 @@ class FlatBuffers:
 
     def load_grads(self, step: int):
         for k in range(len(self.w.tensors)):
-            self.g[k].copy_(draw_grad(self.w, k, step, self.device).reshape(-1))
+            self.g[k].copy_(draw_grad(self.w, k, step, self.device, self.shard_rank).reshape(-1))
 
     def gaps(self):
         """(start, end) element ranges between and after the tensor views."""

@@ -34,19 +34,29 @@ def _normal(shape, std: float, seed: int, device, dtype) -> torch.Tensor:
     return x if dtype == torch.float32 else x.to(dtype)
 
 
-def draw_param(w: Workload, k: int, device="cpu") -> torch.Tensor:
+def _kind(w: Workload, k: int, kind: str, shard_rank: int) -> str:
+    """Seed kind of tensor k.  With shard_rank r > 0, a sharded tensor (one
+    the list flags as owned; a replicated one is the same on every rank) is
+    rank r's own shard and gets its own values; rank 0 draws what a single
+    GPU draws."""
+    if shard_rank and w.tensors[k].owned:
+        return f"{kind}/rank{shard_rank}"
+    return kind
+
+
+def draw_param(w: Workload, k: int, device="cpu", shard_rank: int = 0) -> torch.Tensor:
     """fp32 weight k of the workload, N(0, param_std)."""
-    return _normal(w.tensors[k].shape, w.param_std, tensor_seed(w.seed, "param", 0, k), device,
-                   torch.float32)
+    return _normal(w.tensors[k].shape, w.param_std, tensor_seed(w.seed, _kind(w, k, "param", shard_rank), 0, k),
+                   device, torch.float32)
 
 
-def draw_grad(w: Workload, k: int, step: int, device="cpu") -> torch.Tensor:
+def draw_grad(w: Workload, k: int, step: int, device="cpu", shard_rank: int = 0) -> torch.Tensor:
     """Gradient k of step `step` in its grad dtype (zeros if zero_grad)."""
     t = w.tensors[k]
     dt = _DTYPES[t.grad_dtype]
     if t.zero_grad:
         return torch.zeros(t.shape, device=device, dtype=dt)
-    return _normal(t.shape, w.grad_std, tensor_seed(w.seed, "grad", step, k), device, dt)
+    return _normal(t.shape, w.grad_std, tensor_seed(w.seed, _kind(w, k, "grad", shard_rank), step, k), device, dt)
 
 
 def draw_params(w: Workload, device="cpu") -> list:
