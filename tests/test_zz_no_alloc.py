@@ -1,4 +1,4 @@
-"""soma_clip_norm_noalloc against the regular step.
+"""soma_clip_norm_noalloc against the fp64 oracle and the regular step.
 
 The library's regular entry points allocate device memory on first use.  Some
 callers cannot allow that: an application whose own allocator owns the device
@@ -6,21 +6,28 @@ heap (an extra cudaMalloc fails or fragments its pool), or a latency-critical
 loop where cudaMalloc/cudaFree, which can synchronise the device, are not
 allowed.  soma_clip_norm_noalloc gives them the norm and clip coefficient
 using only a fixed scratch array inside the library.  Here it is called through
-the C ABI twice in a row, on two different lists, and each result is compared
-with the norm and coefficient that soma_opt_step computes on the same inputs.
+the C ABI on three lists in a row, with nothing in between, and each result
+{norm, c} is compared with the oracle's global norm and clip coefficient, and
+with what soma_opt_step computes on the same inputs.  The lists cover bf16
+gradients with replicated entries, fp32 gradients with frozen and all-zero
+entries, and fp16 gradients placed off the 16-byte grid (odd element shifts),
+so that the table's unaligned heads are used.
 
 The file name puts it last in collection order, so a run that stops at its
 first failure has run every other test before this one.
 """
 import ctypes
+import dataclasses
 import math
 
 import pytest
 import torch
 
 import workloads as W
-from parity_harness import NORM_RTOL, DeviceList, make_opt
+from parity_harness import NORM_RTOL, DeviceList, make_opt, make_oracle
 from tensor_grad_clip_gb300 import _abi, build
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -29,6 +36,7 @@ pytestmark = pytest.mark.gpu
 def _built():
     build.build()
     _abi.load()
+    oracle.lib()
 
 
 def _noalloc(tl, divisor, max_norm, out):
@@ -36,38 +44,57 @@ def _noalloc(tl, divisor, max_norm, out):
     return _abi.soma_clip_norm_noalloc(0, tl.pointer(), tl.n, divisor, max_norm, out.data_ptr(), stream)
 
 
-def _case(w):
-    params = W.draw_params(w, "cpu")
-    dl = DeviceList(w, params)
-    dl.load_grads(W.draw_grads(w, 1, "cpu"))
-    return dl
+def _f16_list():
+    w = W.with_steps(W.SMALL["action_expert"](), 1)
+    return dataclasses.replace(w, name=w.name + "-f16",
+                               tensors=tuple(dataclasses.replace(t, grad_dtype=W.F16) for t in w.tensors))
 
 
-def test_two_calls_in_a_row_match_the_step():
+def test_calls_in_a_row_match_the_oracle_and_the_step():
     lists = [W.with_steps(W.SMALL["hsdp_shard"](), 1),   # bf16, replicated entries
-             W.with_steps(W.SMALL["many_small"](), 1)]   # fp32, frozen and all-zero entries
-    cases = [_case(w) for w in lists]
-    out = torch.full((2,), float("nan"), dtype=torch.float64, device="cuda")
-    for w, dl in zip(lists, cases):
-        snap = dl.snapshot()
-        p_before = [x.clone() for x in dl.p]
+             W.with_steps(W.SMALL["many_small"](), 1),   # fp32, frozen and all-zero entries
+             _f16_list()]                                # fp16, gradients off the 16-byte grid
+    shifts = [None, None, [(0, 1 + k % 7, 0, 0) for k in range(len(lists[2].tensors))]]
+    cases = []
+    for w, sh in zip(lists, shifts):
+        params = W.draw_params(w, "cpu")
+        grads = W.draw_grads(w, 1, "cpu")
+        dl = DeviceList(w, params, shift=sh)
+        dl.load_grads(grads)
+        cases.append((w, params, grads, dl))
+    outs = [torch.full((2,), float("nan"), dtype=torch.float64, device="cuda") for _ in lists]
+    snaps = [dl.snapshot() for _, _, _, dl in cases]
+    p_before = [[x.clone() for x in dl.p] for _, _, _, dl in cases]
+    # the calls back to back on one stream: each reuses the scratch the previous one left
+    for (w, _, _, dl), out in zip(cases, outs):
         assert _noalloc(dl.tl, w.grad_divisor, w.max_norm, out) == _abi.SOMA_OK
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    for (w, params, grads, dl), out, snap, pb in zip(cases, outs, snaps, p_before):
         got_norm, got_coef = out.cpu().tolist()
         dl.check_snapshot(snap)
-        assert all(torch.equal(a, b) for a, b in zip(p_before, dl.p))  # nothing updated
+        dl.check_guards()
+        assert all(torch.equal(a, b) for a, b in zip(pb, dl.p))  # nothing updated
+        # the oracle: global norm over trainable, owned entries, then c
+        rn = make_oracle(w, params).global_norm(grads, w.grad_divisor)
+        rc = oracle.clip_coef(rn, w.max_norm)
+        assert rn > 0
+        assert math.isclose(got_norm, rn, rel_tol=NORM_RTOL), (w.name, got_norm, rn)
+        assert math.isclose(got_coef, rc, rel_tol=NORM_RTOL), (w.name, got_coef, rc)
+        if rc == 1.0:
+            assert got_coef == 1.0
+        # the regular step on the same inputs (its chunks differ: equal within the tolerance)
         opt = make_opt(w)
         opt.step(dl.tl, w.grad_divisor, w.max_norm)
         norm, coef, _ = opt.get_norm()
         opt.close()
         assert math.isclose(got_norm, norm, rel_tol=NORM_RTOL), (w.name, got_norm, norm)
         assert math.isclose(got_coef, coef, rel_tol=NORM_RTOL), (w.name, got_coef, coef)
-        assert norm > 0
 
 
 def test_oversized_list_is_refused_before_any_work():
-    # 100 000 one-element entries need about 4.8 MB of segment table, more
-    # than the 4 MiB array; every entry points into real device memory.
+    # 100 000 one-element entries need 100 000 segments of 64 bytes (6.4 MB)
+    # in the segment table alone, more than the 4 MiB array; every entry
+    # points into real device memory.
     n = 100_000
     buf = torch.zeros(n, dtype=torch.float32, device="cuda")
     arr = (_abi.soma_tensor_t * n)()
@@ -77,9 +104,11 @@ def test_oversized_list_is_refused_before_any_work():
         e.param = e.exp_avg = e.exp_avg_sq = base + 4 * k
         e.grad = base + 4 * k
         e.numel, e.group, e.grad_dtype, e.trainable, e.owned = 1, 0, _abi.SOMA_DTYPE_F32, 1, 1
-    out = torch.zeros(2, dtype=torch.float64, device="cuda")
+    out = torch.full((2,), -1.0, dtype=torch.float64, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     st = _abi.soma_clip_norm_noalloc(0, ctypes.cast(arr, ctypes.POINTER(_abi.soma_tensor_t)), n, 1.0, 1.0,
                                      out.data_ptr(), stream)
     assert st == _abi.SOMA_ERR_LIMIT
+    torch.cuda.synchronize()
+    assert out.cpu().tolist() == [-1.0, -1.0]  # nothing was enqueued
     assert _abi.soma_clip_norm_noalloc(0, None, 0, 1.0, 1.0, None, stream) == _abi.SOMA_ERR_INVALID_ARG
