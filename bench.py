@@ -2,20 +2,26 @@
 """Throughput of the fused normalize -> global-norm clip -> AdamW step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload action_expert|hsdp_shard|flat|many_small|tiny]
+                    [--workload hsdp_shard|action_expert|flat|many_small|tiny]
+                    [--per-config LIST]
 
 A step is one soma_opt_step over the whole tensor list (square-sum kernel +
-fused update kernel).  Default workload: the 18-block action-expert list
-(302,008,320 fp32 parameters, bf16 gradients, 144 tensors, 2 groups,
-divisor 64, max_norm 1).  Inputs are synthetic and resident in HBM; p, m and v
-are 1.2 GB each, far above the 129 MB L2, so no flush is needed between steps.
+fused update kernel).  Default workload: the 7B-parameter HSDP shard view
+(32 blocks at width 4096, MLP 11008: 256 tensors, 6,476,136,448 fp32
+parameters, bf16 gradients, a quarter of the tensors replicated, 2 groups,
+divisor 128, max_norm 1), the largest list that fits one GPU.  Inputs are
+synthetic and resident in HBM; p, m and v far exceed the 129 MB L2, so no
+flush is needed between steps.
 
 Prints one JSON line (rank 0): value = trainable parameter elements updated
 per second over all ranks, plus the effective HBM bandwidth under the stated
 accounting (28 B per element with bf16 gradients, 32 B with fp32), a
 roofline entry for the update kernel, the oracle's CPU throughput, an
 end-to-end number through the C ABI with host-resident gradients, and the SM
-clocks seen during the timed region.
+clocks seen during the timed region.  `per_config` holds the same
+device-side measurement for the other lists (by default the action-expert,
+flat, 20 000-tensor and tiny lists), each set up after the previous list's
+buffers were freed, in the same process.
 
 --impl reference times the fp64 CPU oracle (the only other implementation of
 this step available here) on bounded samples of the same workload.
@@ -39,18 +45,23 @@ METRIC = "param-elements updated/sec and effective HBM GB/s (% of GB300 peak) pe
 UNIT = "param-elements/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
-PROFILE_JSON = os.path.join(ROOT, "profiles", "update_kernel_action_expert.json")
+DEFAULT_WORKLOAD = "hsdp_shard"
+DEFAULT_PER_CONFIG = "action_expert,flat,many_small,tiny"
+PER_CONFIG_MIN_S = 0.5   # timed seconds per per-config list, at least
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1, help="GPUs (one rank each under torchrun)")
-    ap.add_argument("--steps", type=int, default=1000, help="timed steps")
+    ap.add_argument("--steps", type=int, default=200, help="timed steps")
     ap.add_argument("--warmup", type=int, default=20, help="untimed steps first")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
                     help="reference: the fp64 CPU oracle on bounded samples of the same list")
-    ap.add_argument("--workload", default="action_expert",
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="tiny, action_expert, many_small, hsdp_shard or flat")
+    ap.add_argument("--per-config", default=None,
+                    help="comma-separated further workloads measured after the main one, device side only "
+                         f"(default with the default workload: {DEFAULT_PER_CONFIG}; 'none' = skip)")
     ap.add_argument("--e2e-steps", type=int, default=20,
                     help="steps per end-to-end window (gradients uploaded from pinned host memory)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end runs")
@@ -202,11 +213,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload_name):
+def profile_json(key):
+    """Committed ncu traffic record of the update kernel on workload `key`."""
+    return os.path.join(ROOT, "profiles", f"update_kernel_{key}.json")
+
+
+def ncu_traffic(key, workload_name):
     """DRAM bytes per update-kernel launch from the committed ncu summary,
     if it was taken on this workload and on the current kernel source."""
     try:
-        with open(PROFILE_JSON) as f:
+        with open(profile_json(key)) as f:
             d = json.load(f)
     except Exception:
         return None
@@ -353,7 +369,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def e2e_runs(args, w, fb, tl, step_on, stream, device, barrier, world):
+def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
     """The step through the public API with the gradients arriving from
     pinned host memory every step, timed twice:
 
@@ -376,7 +392,7 @@ def e2e_runs(args, w, fb, tl, step_on, stream, device, barrier, world):
     G2 = G.clone()
     tl2 = TensorList(fb.p, [G2[fb.offsets[k]:fb.offsets[k] + t.numel] for k, t in enumerate(w.tensors)], fb.m,
                      fb.v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
-                     owned=[t.owned for t in w.tensors], params_lowp=fb.plow)
+                     owned=owned, params_lowp=fb.plow)
     bufs = [(G, tl), (G2, tl2)]
     cs = torch.cuda.Stream(device)
     copied = [torch.cuda.Event() for _ in bufs]
@@ -457,36 +473,67 @@ def e2e_runs(args, w, fb, tl, step_on, stream, device, barrier, world):
             "serial": {"value": elems / (s_ms / 1e3), "ms_per_step": s_ms, "windows_ms_per_step": s_all}}
 
 
-def run_ours(args):
+def kernel_bytes(w):
+    """Algorithmic bytes of one update launch (g 2/4 B, p, m, v read and
+    written: 26/28 B per trainable element, +2 B with a 16-bit model copy) and
+    of one square-sum launch (each owned gradient read once)."""
+    gsz = lambda t: 4 if t.grad_dtype == "f32" else 2
+    upd = sum(t.numel * (gsz(t) + 24 + (2 if t.param_lowp else 0)) for t in w.tensors if t.trainable)
+    nrm = sum(t.numel * gsz(t) for t in w.tensors if t.trainable and t.owned)
+    return upd, nrm
+
+
+class Setup:
+    """One list on the device: flat buffers, a handle with the list's groups,
+    and the tensor list.  Under several ranks each rank holds its own shards
+    of the sharded tensors (own seeds) and the replicated ones, and owns a
+    replicated tensor only if it is that tensor's round-robin owner, so the
+    global norm counts every entry once."""
+
+    def __init__(self, args, w, local, rank, world):
+        import workloads as W
+        from tensor_grad_clip_gb300 import SomaOpt, TensorList
+        from tensor_grad_clip_gb300.sharded import owned_flags
+        self.w = w
+        self.fb = W.FlatBuffers(w, torch_device(local), shard_rank=rank if world > 1 else 0)
+        self.owned = ([t.owned for t in w.tensors] if world == 1
+                      else owned_flags(len(w.tensors), rank, world, [t.owned for t in w.tensors]))
+        self.opt = SomaOpt(local)
+        for q in w.groups:
+            self.opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+        if args.tuning:
+            self.opt.set_tuning(*(int(x) for x in args.tuning.split(",")))
+        if args.single_launch != -1:
+            self.opt.set_single_launch(args.single_launch)
+        fb = self.fb
+        self.tl = TensorList(fb.p, fb.g, fb.m, fb.v, groups=[t.group for t in w.tensors],
+                             trainable=[t.trainable for t in w.tensors], owned=self.owned, params_lowp=fb.plow)
+
+    def close(self):
+        import torch
+        self.opt.close()
+        del self.fb, self.tl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def torch_device(local):
+    import torch
+    return torch.device("cuda", local)
+
+
+def measure(args, S, stream, world, steps, warmup, graph_mode, timing_steps):
+    """Warm-up steps, then `steps` timed steps between CUDA events on the
+    step's stream (a barrier and a device synchronize on both sides, the
+    maximum over ranks), with the SM clocks sampled meanwhile; then a pass
+    with the handle's kernel timing on for per-kernel durations."""
     import torch
     import torch.distributed as dist
-    world, rank, local = dist_env()
-    if world > 1:
-        dist.init_process_group(backend="nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    from tensor_grad_clip_gb300 import SomaOpt, TensorList
-    import tensor_grad_clip_gb300
-    import workloads as W
-    tensor_grad_clip_gb300.load()
-
-    w = workload(args.workload, args.blocks, args.master)
-    fb = W.FlatBuffers(w, device)
-    p, g, m, v = fb.p, fb.g, fb.m, fb.v
-    opt = SomaOpt(local)
-    for q in w.groups:
-        opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
-    if args.tuning:
-        opt.set_tuning(*(int(x) for x in args.tuning.split(",")))
-    if args.single_launch != -1:
-        opt.set_single_launch(args.single_launch)
-    tl = TensorList(p, g, m, v, groups=[t.group for t in w.tensors], trainable=[t.trainable for t in w.tensors],
-                    owned=[t.owned for t in w.tensors], params_lowp=fb.plow)
-    stream = torch.cuda.current_stream(device)
+    w, opt, tl = S.w, S.opt, S.tl
+    device = stream.device
     sharded_step = None
     if world > 1:
-        # each rank holds its own shard of the list; the ranks exchange one
-        # float64 per step (their owned square-sums) for the global norm
+        # one float64 per rank per step (the owned square-sums) for the global norm
         from tensor_grad_clip_gb300.sharded import ShardedStep
         sharded_step = ShardedStep(opt)
 
@@ -497,17 +544,17 @@ def run_ours(args):
             opt.step(lst, w.grad_divisor, w.max_norm, stream)
         return opt
 
-    def one_step():
-        step_on(tl)
-
-    torch.cuda.synchronize()
-
     def barrier():
         if world > 1:
             dist.barrier()
 
+    def set_lrs(t):
+        for q, lr in enumerate(w.group_lrs(t)):
+            opt.set_lr(q, lr)
+
+    torch.cuda.synchronize()
     graph = None
-    if args.graph:
+    if graph_mode:
         # one step captured on a side stream; replays read lr and step counts
         # from the library's device table
         opt.push_groups(stream)
@@ -519,31 +566,28 @@ def run_ours(args):
             with torch.cuda.graph(graph, stream=side):
                 opt.step_graph(tl, w.grad_divisor, w.max_norm, side)
         torch.cuda.synchronize()
-        for i in range(args.warmup):
+        for i in range(warmup):
             graph.replay()
     else:
-        for i in range(args.warmup):
-            lrs = w.group_lrs(i + 1)
-            for q, lr in enumerate(lrs):
-                opt.set_lr(q, lr)
-            one_step()
+        for i in range(warmup):
+            set_lrs(i % w.steps + 1)
+            step_on(tl)
     torch.cuda.synchronize()
     plan = opt.plan()
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(device.index)
     sampler.start()
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         if graph is not None:
             graph.replay()
             continue
         if w.lr_at is not None:
-            for q, lr in enumerate(w.group_lrs(i % w.steps + 1)):
-                opt.set_lr(q, lr)
-        one_step()
+            set_lrs(i % w.steps + 1)
+        step_on(tl)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -559,77 +603,158 @@ def run_ours(args):
     if graph is None:
         opt.set_timing(True)
         opt.read_timing()
-        for i in range(min(args.steps, 300)):
-            one_step()
+        for i in range(min(steps, timing_steps)):
+            step_on(tl)
         torch.cuda.synchronize()
         norm_ms, upd_ms, nsteps = opt.read_timing()
         opt.set_timing(False)
+    # The square-sum kernel on its own, launched back to back (soma_opt_sumsq
+    # runs the step's first kernel and stores the square-sum): events around
+    # a single launch also time the gap before it starts, which is a large
+    # part of a 0.1 ms launch.
+    chained_ms = None
+    if graph is None and world == 1 and timing_steps > 0:
+        out = torch.zeros(1, dtype=torch.float64, device=device)
+        opt.sumsq(tl, w.grad_divisor, out, stream)
+        n_chain = max(5, min(steps, timing_steps))
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(n_chain):
+            opt.sumsq(tl, w.grad_divisor, out, stream)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        chained_ms = c0.elapsed_time(c1) / n_chain
+        step_on(tl)  # leave the handle's last result a full step's
     if world > 1:
         t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     norm, coef, nonfinite = opt.get_norm(stream)
+    if graph is not None:  # no per-kernel events inside a graph: attribute the whole step
+        upd_ms, norm_ms, nsteps = elapsed_ms, 0.0, steps
+        del graph
+    return {"elapsed_ms": elapsed_ms, "steps": steps, "plan": plan, "clocks": clocks, "norm_ms": norm_ms,
+            "upd_ms": upd_ms, "timing_steps": nsteps, "norm_chained_ms": chained_ms, "norm": norm, "coef": coef,
+            "nonfinite": nonfinite, "step_on": step_on, "barrier": barrier}
 
-    ms_per_step = elapsed_ms / args.steps
-    elems = w.trainable_numel
-    value = elems * world * args.steps / (elapsed_ms / 1e3)
+
+def summarize(w, r, world, hbm_peak):
+    """Throughput and bandwidth figures of one measured list."""
+    ms = r["elapsed_ms"] / r["steps"]
+    eff = w.effective_bytes_per_step() / (ms / 1e3) / 1e9
+    alg = w.algorithmic_bytes_per_step() / (ms / 1e3) / 1e9
+    upd_bytes, norm_bytes = kernel_bytes(w)
+    n = max(r["timing_steps"], 1)
+    upd_ms, norm_ms = r["upd_ms"] / n, r["norm_ms"] / n
+    return {
+        "ms_per_step": ms, "steps": r["steps"],
+        "value": w.trainable_numel * world / (ms / 1e3),
+        "effective_hbm_gbs": eff * world, "effective_hbm_frac_of_peak": eff / hbm_peak,
+        "effective_hbm_frac_of_8tbs": eff / 8000.0,
+        "algorithmic_hbm_gbs": alg * world, "algorithmic_hbm_frac_of_8tbs": alg / 8000.0,
+        "update_kernel_ms": upd_ms, "norm_kernel_ms": norm_ms,
+        "update_kernel_gbs": upd_bytes / (upd_ms / 1e3) / 1e9 if upd_ms > 0 else None,
+        "norm_kernel_gbs": norm_bytes / (norm_ms / 1e3) / 1e9 if norm_ms > 0 and world == 1 else None,
+        "norm_kernel_chained_ms": r["norm_chained_ms"],
+        "norm_kernel_chained_gbs": norm_bytes / (r["norm_chained_ms"] / 1e3) / 1e9 if r["norm_chained_ms"] else None,
+        "launches_per_step": r["plan"]["launches_per_step"],
+        "clocks": r["clocks"], "last_norm": r["norm"], "last_clip_coef": r["coef"], "nonfinite": r["nonfinite"],
+    }
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import tensor_grad_clip_gb300
+    tensor_grad_clip_gb300.load()
     hbm_peak, peak_kind, _ = peaks()
-    eff_gbs = w.effective_bytes_per_step() / (ms_per_step / 1e3) / 1e9
-    alg_gbs = w.algorithmic_bytes_per_step() / (ms_per_step / 1e3) / 1e9
+    stream = torch.cuda.current_stream(device)
+
+    w = workload(args.workload, args.blocks, args.master)
+    S = Setup(args, w, local, rank, world)
+    r = measure(args, S, stream, world, args.steps, args.warmup, args.graph, 300)
+    head = summarize(w, r, world, hbm_peak)
+    plan = r["plan"]
 
     # dominant kernel: the fused update (26 B/elem bf16 grads, 28 B/elem fp32)
-    gsz = lambda t: 4 if t.grad_dtype == "f32" else 2
-    upd_bytes = sum(t.numel * (gsz(t) + 24 + (2 if t.param_lowp else 0)) for t in w.tensors if t.trainable)
-    norm_bytes = sum(t.numel * gsz(t) for t in w.tensors if t.trainable and t.owned)
-    if graph is not None:  # no per-kernel events inside a graph: attribute the whole step
-        upd_ms, norm_ms, nsteps = elapsed_ms, 0.0, args.steps
-    upd_avg_ms = upd_ms / max(nsteps, 1)
-    norm_avg_ms = norm_ms / max(nsteps, 1)
+    upd_bytes, norm_bytes = kernel_bytes(w)
+    upd_avg_ms, norm_avg_ms = head["update_kernel_ms"], head["norm_kernel_ms"]
     achieved = upd_bytes / (upd_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "update_kernel", "achieved": achieved, "peak": hbm_peak,
                 "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                "traffic": ncu_traffic(w.name), "algorithmic_bytes_per_launch": upd_bytes,
-                "avg_launch_ms": upd_avg_ms,
-                "norm_kernel": {"achieved": norm_bytes / (norm_avg_ms / 1e3) / 1e9
-                                if norm_avg_ms > 0 and world == 1 else None,
-                                "avg_launch_ms": norm_avg_ms, "algorithmic_bytes_per_launch": norm_bytes}}
+                "traffic": ncu_traffic(args.workload, w.name) if not (args.blocks or args.master) else None,
+                "algorithmic_bytes_per_launch": upd_bytes, "avg_launch_ms": upd_avg_ms,
+                "norm_kernel": {"achieved": head["norm_kernel_gbs"], "avg_launch_ms": norm_avg_ms,
+                                "algorithmic_bytes_per_launch": norm_bytes,
+                                "note": "events around each launch in the kernel-timing pass (they also time the "
+                                        "gap before the launch starts); chained: the same kernel launched back to "
+                                        "back through soma_opt_sumsq",
+                                "chained_launch_ms": head["norm_kernel_chained_ms"],
+                                "achieved_chained": head["norm_kernel_chained_gbs"]}}
     if world > 1:
         roofline["norm_kernel"]["note"] = ("several ranks: the square-sum runs in soma_opt_sumsq before the "
                                            "all-gather; the events time the finish kernel")
 
     e2e = None
-    if not args.no_e2e and graph is None:
+    if not args.no_e2e and not args.graph:
         # End to end through the C ABI: every step copies that step's gradients
         # from pinned host memory into a device gradient buffer, runs the step
         # and reads the norm back to the host.
-        e2e = e2e_runs(args, w, fb, tl, step_on, stream, device, barrier, world)
+        e2e = e2e_runs(args, w, S.fb, S.tl, S.owned, r["step_on"], stream, device, r["barrier"], world)
+    S.close()
+    del S
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
         cpu["all_cores"] = cpu_baseline_all_cores(w)
 
+    # The other lists, device side only, each on a fresh handle after the
+    # previous list's buffers were freed.  Each is timed for at least
+    # PER_CONFIG_MIN_S seconds (and at least --steps steps).
+    per = {}
+    names = args.per_config
+    if names is None:
+        names = DEFAULT_PER_CONFIG if (args.workload == DEFAULT_WORKLOAD and not args.blocks) else "none"
+    for name in [x for x in names.split(",") if x and x != "none" and x != args.workload]:
+        wk = workload(name)
+        Sk = Setup(args, wk, local, rank, world)
+        probe = measure(args, Sk, stream, world, max(3, args.warmup), max(3, args.warmup), False, 0)
+        est_ms = probe["elapsed_ms"] / probe["steps"]
+        k = max(args.steps, min(20000, int(PER_CONFIG_MIN_S * 1e3 / max(est_ms, 1e-3)) + 1))
+        rk = measure(args, Sk, stream, world, k, 0, False, min(k, 300))
+        per[name] = {"config": describe(wk)} | summarize(wk, rk, world, hbm_peak)
+        Sk.close()
+        del Sk
+
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": describe(w) | {"parallelism": f"shard group x{world}: one all-gather of 8 B per rank per step"
                                      if world > 1 else "single GPU",
-                                     "mode": "CUDA-graph replay of one step" if graph is not None
+                                     "mode": "CUDA-graph replay of one step" if args.graph
                                      else "soma_opt_step per step", "plan": plan},
-            "effective_hbm_gbs": eff_gbs * world,
-            "effective_hbm_frac_of_peak": eff_gbs / hbm_peak,
-            "effective_hbm_frac_of_8tbs": eff_gbs / 8000.0,
-            "algorithmic_hbm_gbs": alg_gbs * world,
+            "effective_hbm_gbs": head["effective_hbm_gbs"],
+            "effective_hbm_frac_of_peak": head["effective_hbm_frac_of_peak"],
+            "effective_hbm_frac_of_8tbs": head["effective_hbm_frac_of_8tbs"],
+            "algorithmic_hbm_gbs": head["algorithmic_hbm_gbs"],
+            "algorithmic_hbm_frac_of_8tbs": head["algorithmic_hbm_frac_of_8tbs"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             # multi-rank steps add the finish kernel (rank-ordered sum of the ranks' square-sums)
             "gpu_launches": (plan["launches_per_step"] + (1 if world > 1 else 0)) * args.steps,
-            "clocks": clocks,
-            "last_norm": norm, "last_clip_coef": coef, "nonfinite": nonfinite,
+            "clocks": head["clocks"],
+            "last_norm": head["last_norm"], "last_clip_coef": head["last_clip_coef"],
+            "nonfinite": head["nonfinite"],
+            "per_config": per or None,
         }
         print(json.dumps(line), flush=True)
-    opt.close()
     if world > 1:
         dist.destroy_process_group()
 

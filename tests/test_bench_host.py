@@ -40,11 +40,22 @@ def test_code_only_hash_ignores_comments_and_layout():
 
 
 def test_traffic_is_reported_only_for_the_code_and_list_it_was_measured_on():
-    with open(bench.PROFILE_JSON) as f:
+    with open(bench.profile_json("action_expert")) as f:
         rec = json.load(f)
-    got = bench.ncu_traffic(W.FULL["action_expert"]().name)
+    got = bench.ncu_traffic("action_expert", W.FULL["action_expert"]().name)
     if rec["kernel_sha"] == bench.kernel_source_hash():
         assert got == rec["dram_bytes_per_launch"]
     else:  # the kernels changed since the capture: no traffic figure
         assert got is None
-    assert bench.ncu_traffic(W.FULL["flat"]().name) is None
+    # a record names its list: another list's name finds nothing
+    assert bench.ncu_traffic("action_expert", W.FULL["flat"]().name) is None
+    assert bench.ncu_traffic("no_such_list", W.FULL["flat"]().name) is None
+
+
+def test_default_line_is_the_largest_single_gpu_list():
+    # the 7B shard view is the largest list that fits one GPU; the others
+    # are measured in the same run under per_config
+    assert bench.DEFAULT_WORKLOAD == "hsdp_shard"
+    sizes = {k: f().trainable_numel for k, f in W.FULL.items()}
+    assert max(sizes, key=sizes.get) == "hsdp_shard"
+    assert set(bench.DEFAULT_PER_CONFIG.split(",")) == set(W.FULL) - {"hsdp_shard"}
