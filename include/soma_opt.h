@@ -397,7 +397,7 @@ void soma_opt_destroy(soma_opt_t opt);
  * and partial sums do not fit returns SOMA_ERR_LIMIT before anything is
  * enqueued.  Each owned entry takes at least one 64-byte segment, and a list
  * is cut into at most about 32 768 chunks of at least 32 Ki elements, so at
- * least 26 000 owned entries fit whatever their sizes (about 64 000 when they
+ * least 26 000 owned entries fit whatever their sizes (about 65 000 when they
  * are small enough to share chunks).
  *
  * Blocking: each call copies the tables from a host buffer that the next call

@@ -333,3 +333,34 @@ def test_state_dict_round_trip():
         c.load_state_dict(state)
     for o in (a, b, c):
         o.close()
+
+
+def _noalloc_list(numels, dtype=_abi.SOMA_DTYPE_F32):
+    """Entries at distinct fake 256-byte-aligned addresses (never dereferenced:
+    the size check runs before any CUDA call)."""
+    arr = (_abi.soma_tensor_t * len(numels))()
+    addr = 1 << 40
+    for k, n in enumerate(numels):
+        e = arr[k]
+        e.param = e.exp_avg = e.exp_avg_sq = e.grad = addr
+        e.numel, e.group, e.grad_dtype, e.trainable, e.owned = n, 0, dtype, 1, 1
+        addr += (n * 4 + 255) // 256 * 256
+    return ctypes.cast(arr, ctypes.POINTER(_abi.soma_tensor_t)), arr
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="a list that fits would be launched on fake pointers")
+def test_noalloc_capacity_matches_the_header():
+    # The header promises at least 26 000 owned entries of any sizes (one
+    # 2^40-element entry forces the most chunks a list can have, 32 768 full
+    # ones, plus the tiny entries' own segments) and about 65 000 tiny ones.
+    # A list that fits passes the size check and then fails on this machine's
+    # missing GPU (SOMA_ERR_CUDA); one that does not fit gets SOMA_ERR_LIMIT.
+    out = 1 << 41  # 8-byte aligned, never written: no device here
+    def status(numels):
+        ptr, keep = _noalloc_list(numels)
+        return _abi.soma_clip_norm_noalloc(0, ptr, len(numels), 1.0, 1.0, out, None)
+    assert status([1 << 40] + [1] * 25_999) == _abi.SOMA_ERR_CUDA
+    assert status([1 << 40] + [1] * 26_599) == _abi.SOMA_ERR_LIMIT
+    assert status([1] * 65_000) == _abi.SOMA_ERR_CUDA
+    assert status([1] * 65_400) == _abi.SOMA_ERR_LIMIT
+    assert status([1 << 20] * 26_000) == _abi.SOMA_ERR_CUDA  # 26 000 entries of 1 Mi elements each
