@@ -87,6 +87,18 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x, device):
+    """Largest value of x over the ranks (x itself on one rank).  NCCL
+    reduces device tensors, gloo host ones."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -384,7 +396,6 @@ def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
     the next step is enqueued; only the next upload is already queued then.
     Each mode is timed over three windows and the median window reported."""
     import torch
-    import torch.distributed as dist
     from tensor_grad_clip_gb300 import TensorList
     G = fb.G
     host_g = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
@@ -439,11 +450,7 @@ def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
         torch.cuda.synchronize()
         barrier()
         ms = max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3)
-        if world > 1:
-            x = torch.tensor([ms], device=device, dtype=torch.float64)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            ms = float(x.item())
-        return ms
+        return max_over_ranks(ms, device)
 
     # the host link on its own: one gradient upload, no kernels
     torch.cuda.synchronize()
@@ -625,10 +632,7 @@ def measure(args, S, stream, world, steps, warmup, graph_mode, timing_steps):
         torch.cuda.synchronize()
         chained_ms = c0.elapsed_time(c1) / n_chain
         step_on(tl)  # leave the handle's last result a full step's
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device)
     norm, coef, nonfinite = opt.get_norm(stream)
     if graph is not None:  # no per-kernel events inside a graph: attribute the whole step
         upd_ms, norm_ms, nsteps = elapsed_ms, 0.0, steps
@@ -667,7 +671,11 @@ def run_ours(args):
     import torch.distributed as dist
     world, rank, local = dist_env()
     if world > 1:
-        dist.init_process_group(backend="nccl", init_method="env://")
+        # one rank per GPU over NCCL; ranks that share a GPU (fewer GPUs than
+        # ranks: NCCL refuses two ranks on one device) exchange over gloo
+        backend = "nccl" if torch.cuda.device_count() >= world else "gloo"
+        dist.init_process_group(backend=backend, init_method="env://")
+        local = local % torch.cuda.device_count()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     import tensor_grad_clip_gb300
@@ -737,7 +745,8 @@ def run_ours(args):
             "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": describe(w) | {"parallelism": f"shard group x{world}: one all-gather of 8 B per rank per step"
+            "config": describe(w) | {"parallelism": f"shard group x{world}: one all-gather of 8 B per rank per step "
+                                                    f"({dist.get_backend()}, {torch.cuda.device_count()} GPUs)"
                                      if world > 1 else "single GPU",
                                      "mode": "CUDA-graph replay of one step" if args.graph
                                      else "soma_opt_step per step", "plan": plan},
