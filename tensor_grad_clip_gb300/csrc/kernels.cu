@@ -653,19 +653,27 @@ __device__ __forceinline__ void prefetch_flat(const Seg* segs, const int* vpre) 
     }
 }
 
-__device__ __forceinline__ void prefetch_vectors(const Seg& s) {
+// L2 prefetch of the gradient, p, m and v of vector i of segment s.
+__device__ __forceinline__ void prefetch_vector(const Seg& s, int i) {
+    const int e = s.head + kVec * i;
     const int gsz = s.gdtype == kF32 ? 4 : 2;
-    for (int i = threadIdx.x, n = 0; i < s.nvec && n < kPrefetchVectors; i += blockDim.x, ++n) {
-        const int e = s.head + kVec * i;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(s.g) + (size_t)e * gsz));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(s.p + e));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(s.m + e));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(s.v + e));
-    }
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(s.g) + (size_t)e * gsz));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(s.p + e));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(s.m + e));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(s.v + e));
+}
+
+__device__ __forceinline__ void prefetch_vectors(const Seg& s) {
+    for (int i = threadIdx.x, n = 0; i < s.nvec && n < kPrefetchVectors; i += blockDim.x, ++n) prefetch_vector(s, i);
 }
 
 // A chunk made of one segment (a slice of a large tensor): dtypes fixed at
-// compile time, two vectors in flight per thread.
+// compile time, two vectors in flight per thread.  With 16-bit gradients each
+// thread also prefetches its next pair of vectors into L2 while it loads the
+// current pair, which puts more requests in flight without holding registers.
+// Same-box A/B: the step 0.54 % faster on the 7B shard view and 0.56 % on the
+// action-expert list; with fp32 gradients it was 1 % slower on the flat list,
+// so fp32 gradients go without.
 template <int DT, int LOW>
 __device__ __forceinline__ void segment_update(const Seg& s, const GroupHp& h, float scale) {
     for (int j = threadIdx.x; j < s.head; j += blockDim.x) update_one(s, j, h, scale);
@@ -676,6 +684,10 @@ __device__ __forceinline__ void segment_update(const Seg& s, const GroupHp& h, f
             Lane8 x0, x1;
             load8_w<DT>(s, i, x0);
             load8_w<DT>(s, i + B, x1);
+            if (DT != kF32 && i + 3 * B < n) {
+                prefetch_vector(s, i + 2 * B);
+                prefetch_vector(s, i + 3 * B);
+            }
             compute8_t<DT>(x0, h, scale);
             compute8_t<DT>(x1, h, scale);
             store8_w<LOW>(s, i, x0);
