@@ -364,3 +364,21 @@ def test_noalloc_capacity_matches_the_header():
     assert status([1] * 65_000) == _abi.SOMA_ERR_CUDA
     assert status([1] * 65_400) == _abi.SOMA_ERR_LIMIT
     assert status([1 << 20] * 26_000) == _abi.SOMA_ERR_CUDA  # 26 000 entries of 1 Mi elements each
+
+
+def test_get_segments_arguments_and_state():
+    # the segment tables exist only once a step has built them
+    opt = SomaOpt(0)
+    opt.add_group(lr=1e-3)
+    n = ctypes.c_int64(-1)
+    assert _abi.soma_opt_get_segments(opt.handle, 0, None, 0, ctypes.byref(n)) == _abi.SOMA_ERR_STATE
+    with pytest.raises(SomaError) as e:
+        opt.segments("update")
+    assert e.value.status == _abi.SOMA_ERR_STATE
+    assert _abi.soma_opt_get_segments(opt.handle, 2, None, 0, ctypes.byref(n)) == _abi.SOMA_ERR_INVALID_ARG
+    assert _abi.soma_opt_get_segments(opt.handle, 0, None, 0, None) == _abi.SOMA_ERR_INVALID_ARG
+    assert _abi.soma_opt_get_segments(opt.handle, 0, None, 5, ctypes.byref(n)) == _abi.SOMA_ERR_INVALID_ARG
+    assert _abi.soma_opt_get_segments(opt.handle, 0, None, -1, ctypes.byref(n)) == _abi.SOMA_ERR_INVALID_ARG
+    assert n.value == -1  # nothing written on failure
+    opt.close()
+    assert _abi.soma_opt_get_segments(None, 0, None, 0, ctypes.byref(n)) == _abi.SOMA_ERR_STATE

@@ -160,3 +160,50 @@ def test_pipelined_uploads_equal_serial_steps_bit_for_bit():
         opt.close()
     for k, (a, b) in enumerate(zip(*finals)):
         assert torch.equal(a, b), k
+
+
+@pytest.mark.parametrize("which", ["many_small", "hsdp_shard", "unaligned"])
+def test_segment_tables_tile_every_tensor(which):
+    # soma_opt_get_segments on the list the last step ran: both tables cover
+    # their tensors exactly once, in list order, in chunks of at most 64
+    # segments; a segment's vector body follows its head and is 16-byte
+    # aligned in the gradient.
+    import numpy as np
+    if which == "unaligned":
+        w = _workload(1)
+        shift = [(k % 3, 1 + k % 5, (k + 1) % 2, 0) for k in range(len(w.tensors))]
+    else:
+        w = W.with_steps(W.SMALL[which](), 1)
+        shift = None
+    dl = DeviceList(w, W.draw_params(w, "cpu"), shift=shift)
+    dl.load_grads(W.draw_grads(w, 1, "cpu"))
+    opt = make_opt(w)
+    opt.set_single_launch(0)  # the tables the two kernels use
+    opt.step(dl.tl, w.grad_divisor, w.max_norm)
+    plan = opt.plan()
+    starts = {dl.g[k].data_ptr(): k for k in range(len(w.tensors)) if w.tensors[k].numel}
+    for which_tab, want in (("update", lambda t: t.trainable), ("norm", lambda t: t.trainable and t.owned)):
+        seg = opt.segments(which_tab)
+        assert seg["len"].size == plan[f"{which_tab}_segments"]
+        chunks = seg["chunk"]
+        assert chunks[0] == 0 and np.all(np.diff(chunks) >= 0) and np.all(np.diff(chunks) <= 1)
+        assert chunks[-1] + 1 == plan[f"{which_tab}_chunks"]
+        assert np.bincount(chunks).max() <= 64
+        covered = {}
+        k = -1
+        for a, n, h, nv, grp in zip(seg["grad"], seg["len"], seg["head"], seg["nvec"], seg["group"]):
+            a, n, h, nv, grp = int(a), int(n), int(h), int(nv), int(grp)
+            if a in starts:  # the first segment of a tensor
+                k = starts[a]
+                off = 0
+            esz = dl.g[k].element_size()
+            assert a == dl.g[k].data_ptr() + off * esz, (which_tab, k, off)
+            assert grp == w.tensors[k].group
+            assert 0 <= h <= n and h + 8 * nv <= n
+            if nv:
+                assert (a + h * esz) % 16 == 0
+            off += n
+            covered[k] = off
+        expect = {k: t.numel for k, t in enumerate(w.tensors) if want(t) and t.numel}
+        assert covered == expect, which_tab
+    opt.close()
