@@ -600,6 +600,23 @@ def measure(args, S, stream, world, steps, warmup, graph_mode, timing_steps):
     barrier()
     clocks = sampler.stop()
     elapsed_ms = e0.elapsed_time(e1)
+    # Per-step distribution: a separate pass with an event after every step
+    # (events between steps keep a step's square-sum kernel from starting
+    # under the previous update kernel's tail, so this pass is not the
+    # headline number either).
+    per_step = None
+    if graph is None and timing_steps > 0:
+        n_ps = max(1, min(steps, 50))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ps + 1)]
+        evs[0].record(stream)
+        for i in range(n_ps):
+            if w.lr_at is not None:
+                set_lrs(i % w.steps + 1)
+            step_on(tl)
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        ts = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(n_ps))
+        per_step = {"steps": n_ps, "median_ms": statistics.median(ts), "min_ms": ts[0], "max_ms": ts[-1]}
     # Per-kernel durations for the roofline: a second pass over the same
     # steps with CUDA events recorded between the two kernels (an event there
     # also stops the update kernel from overlapping the square-sum's tail, and
@@ -638,7 +655,8 @@ def measure(args, S, stream, world, steps, warmup, graph_mode, timing_steps):
         upd_ms, norm_ms, nsteps = elapsed_ms, 0.0, steps
         del graph
     return {"elapsed_ms": elapsed_ms, "steps": steps, "plan": plan, "clocks": clocks, "norm_ms": norm_ms,
-            "upd_ms": upd_ms, "timing_steps": nsteps, "norm_chained_ms": chained_ms, "norm": norm, "coef": coef,
+            "upd_ms": upd_ms, "timing_steps": nsteps, "norm_chained_ms": chained_ms, "per_step": per_step,
+            "norm": norm, "coef": coef,
             "nonfinite": nonfinite, "step_on": step_on, "barrier": barrier}
 
 
@@ -651,7 +669,7 @@ def summarize(w, r, world, hbm_peak):
     n = max(r["timing_steps"], 1)
     upd_ms, norm_ms = r["upd_ms"] / n, r["norm_ms"] / n
     return {
-        "ms_per_step": ms, "steps": r["steps"],
+        "ms_per_step": ms, "steps": r["steps"], "per_step_ms": r["per_step"],
         "value": w.trainable_numel * world / (ms / 1e3),
         "effective_hbm_gbs": eff * world, "effective_hbm_frac_of_peak": eff / hbm_peak,
         "effective_hbm_frac_of_8tbs": eff / 8000.0,
@@ -743,7 +761,8 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "per_step_ms": head["per_step_ms"],
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": describe(w) | {"parallelism": f"shard group x{world}: one all-gather of 8 B per rank per step "
                                                     f"({dist.get_backend()}, {torch.cuda.device_count()} GPUs)"

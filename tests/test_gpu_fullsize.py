@@ -6,7 +6,7 @@ Every element, after each chained step:
   10 steps, the fp64 oracle state of every element kept on the host
   (7.2 GB and 36 GB) and updated by the oracle's own per-tensor function on
   slices of 1 Mi elements over a thread pool;
-* the 20 000-tensor list (104 M): 3 steps through the oracle's whole step.
+* the 20 000-tensor list (104 M): 10 steps through the oracle's whole step.
 
 The 7B shard view (6.48 G) would need 155 GB of fp64 state, so it is checked
 over 10 steps on:
@@ -286,10 +286,11 @@ def test_tensor_beyond_2_pow_31_elements():
 
 def test_full_size_many_small_every_element():
     # The 20 000-tensor list at full size (104 M trainable elements), every
-    # element against the oracle after each of 3 chained steps.  The flat
+    # element against the oracle after each of its 10 chained steps.  The flat
     # buffers come back to the host once per step and are sliced per tensor.
     from parity_harness import make_oracle
-    w = W.with_steps(W.FULL["many_small"](), 3)
+    w = W.FULL["many_small"]()
+    assert w.steps == 10
     dev = torch.device("cuda", 0)
     fb = W.FlatBuffers(w, dev, grad_step=1)
     P0 = fb.P.cpu()
