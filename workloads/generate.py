@@ -3,8 +3,10 @@
 Each tensor gets its own generator, seeded from (workload seed, kind, step,
 tensor index), so a tensor's values do not depend on which other tensors are
 drawn or in which order.  Values drawn on the CPU and on a CUDA device differ
-(different generators); every consumer copies the values it needs from the
-tensors actually used, never re-draws them.
+(different generators), so a consumer never takes a CPU draw for values that
+were drawn on a device: it copies them from the tensors actually used, or
+draws them again on the same kind of device, where the same seed gives the
+same values.
 """
 from __future__ import annotations
 
