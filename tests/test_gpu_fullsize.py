@@ -8,8 +8,11 @@ Every element, after each chained step:
   slices of 1 Mi elements over a thread pool;
 * the 20 000-tensor list (104 M): 10 steps through the oracle's whole step.
 
-The 7B shard view (6.48 G) would need 155 GB of fp64 state, so it is checked
-over 10 steps on:
+The 7B shard view (6.48 G) would need 155 GB of fp64 state to check every
+element after each of its 10 steps.  It is checked instead on every element
+after its first step and after its tenth, with each tensor's oracle chain run
+on its own (it depends only on that tensor's state, its gradients and each
+step's clip coefficient), and after each step on:
 
 * every element of its first and last block (16 tensors, both groups, owned
   and replicated ones: 404 M elements);
@@ -263,6 +266,149 @@ def test_full_size_hsdp_shard_blocks_and_every_chunk_boundary():
     plan, checked = run_full(w, steps=10, select=select)
     assert plan["trainable_numel"] == w.trainable_numel
     assert plan["owned_numel"] == w.owned_numel
+
+
+def test_full_size_hsdp_shard_first_step_every_element():
+    # Every element of the 7B shard view after its first step: the oracle
+    # starts from the same seeded weights with zero moments, so each tensor
+    # can be checked on its own, slice by slice, without carrying fp64 state
+    # for the whole list (the 10-step chain above is sampled instead).
+    w = W.FULL["hsdp_shard"]()
+    dev = torch.device("cuda", 0)
+    fb = W.FlatBuffers(w, dev, grad_step=1)
+    opt = SomaOpt(0)
+    for q in w.groups:
+        opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+    tl = TensorList(fb.p, fb.g, fb.m, fb.v, groups=[t.group for t in w.tensors],
+                    trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
+    p0 = [x.cpu() for x in fb.p]
+    host_g = [x.cpu() for x in fb.g]
+    lrs = w.group_lrs(1)
+    for q, lr in enumerate(lrs):
+        opt.set_lr(q, lr)
+    opt.step(tl, w.grad_divisor, w.max_norm)
+    norm, coef, nonfinite = opt.get_norm()
+    pool = ThreadPoolExecutor(POOL)
+    rn = oracle_norm(w, host_g, w.grad_divisor, pool)
+    rc = oracle.clip_coef(rn, w.max_norm)
+    assert not nonfinite
+    assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (norm, rn)
+    assert math.isclose(coef, rc, rel_tol=NORM_RTOL), (coef, rc)
+    checked = 0
+    for k, t in enumerate(w.tensors):
+        q = w.groups[t.group]
+        got = [x.cpu().numpy() for x in (fb.p[k], fb.m[k], fb.v[k])]
+
+        def one(lo, k=k, t=t, q=q, got=got):
+            hi = min(t.numel, lo + SLICE)
+            p_s = p0[k].numpy()[lo:hi].astype(np.float64)
+            m_s, v_s = np.zeros_like(p_s), np.zeros_like(p_s)
+            oracle.adamw_update(p_s, host_g[k][lo:hi], m_s, v_s, lr=lrs[t.group], beta1=q.beta1, beta2=q.beta2,
+                                eps=q.eps, weight_decay=q.weight_decay, step=1, c=rc, divisor=w.grad_divisor)
+            out = []
+            for nm, g_, r_ in zip("pmv", got, (p_s, m_s, v_s)):
+                bad = np.flatnonzero(_bad(g_[lo:hi], r_))
+                if bad.size:
+                    out.append((nm, lo, bad[:1]))
+            return out
+
+        for res in pool.map(one, range(0, t.numel, SLICE)):
+            for nm, lo, where in res:
+                j = lo + int(where[0])
+                raise AssertionError(f"step 1 {t.name} {nm}: element {j} out of tolerance "
+                                     f"(got {got['pmv'.index(nm)][j]!r})")
+        checked += t.numel
+        del got
+    assert checked == w.trainable_numel
+    gbits = torch.int16
+    assert all(torch.equal(fb.g[k].cpu().view(gbits), host_g[k].view(gbits)) for k in range(len(w.tensors)))
+    torch.cuda.synchronize()
+    assert fb.gaps_intact(), "a write landed outside a tensor"
+    opt.close()
+    pool.shutdown()
+    del fb, p0, host_g
+    torch.cuda.empty_cache()
+
+
+def test_full_size_hsdp_shard_ten_steps_every_element():
+    # Every element of the 7B shard view after its 10 chained steps.  Each
+    # tensor's oracle chain depends only on its own weights, its gradients
+    # and each step's clip coefficient, so the GPU runs the whole chain first
+    # (the oracle's norm and c of every step checked and kept), its final
+    # p, m, v come back to the host, and the oracle then replays the chain
+    # tensor by tensor in fp64.  Weights and gradients are drawn again on the
+    # device with the seeds the buffers were filled from (the same values).
+    w = W.FULL["hsdp_shard"]()
+    dev = torch.device("cuda", 0)
+    fb = W.FlatBuffers(w, dev, grad_step=1)
+    opt = SomaOpt(0)
+    for q in w.groups:
+        opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+    tl = TensorList(fb.p, fb.g, fb.m, fb.v, groups=[t.group for t in w.tensors],
+                    trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
+    pool = ThreadPoolExecutor(POOL)
+    coefs = []
+    for s_ in range(1, w.steps + 1):
+        if s_ > 1:
+            fb.load_grads(s_)
+        for q, lr in enumerate(w.group_lrs(s_)):
+            opt.set_lr(q, lr)
+        opt.step(tl, w.grad_divisor, w.max_norm)
+        norm, coef, nonfinite = opt.get_norm()
+        host_g = [x.cpu() for x in fb.g]
+        rn = oracle_norm(w, host_g, w.grad_divisor, pool)
+        del host_g
+        rc = oracle.clip_coef(rn, w.max_norm)
+        assert not nonfinite
+        assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (s_, norm, rn)
+        assert math.isclose(coef, rc, rel_tol=NORM_RTOL), (s_, coef, rc)
+        coefs.append(rc)
+    for q in range(len(w.groups)):
+        assert opt.get_group_step(q) == w.steps
+    torch.cuda.synchronize()
+    assert fb.gaps_intact(), "a write landed outside a tensor"
+    final = [[x.cpu().numpy() for x in (fb.p[k], fb.m[k], fb.v[k])] for k in range(len(w.tensors))]
+    opt.close()
+    del fb, tl
+    torch.cuda.empty_cache()
+
+    checked = 0
+    for k, t in enumerate(w.tensors):
+        q = w.groups[t.group]
+        state = [W.draw_param(w, k, dev).reshape(-1).cpu().numpy().astype(np.float64)]
+        state += [np.zeros_like(state[0]), np.zeros_like(state[0])]
+        slices = range(0, t.numel, SLICE)
+        for s_ in range(1, w.steps + 1):
+            g = W.draw_grad(w, k, s_, dev).reshape(-1).cpu()
+            lr = w.group_lrs(s_)[t.group]
+
+            def upd(lo, s_=s_, g=g, lr=lr, q=q, state=state, n=t.numel):
+                hi = min(n, lo + SLICE)
+                oracle.adamw_update(state[0][lo:hi], g[lo:hi], state[1][lo:hi], state[2][lo:hi], lr=lr,
+                                    beta1=q.beta1, beta2=q.beta2, eps=q.eps, weight_decay=q.weight_decay, step=s_,
+                                    c=coefs[s_ - 1], divisor=w.grad_divisor)
+            list(pool.map(upd, slices))
+            del g
+
+        def cmp(lo, k=k, state=state, n=t.numel):
+            hi = min(n, lo + SLICE)
+            for nm, got, ref in zip("pmv", final[k], state):
+                bad = np.flatnonzero(_bad(got[lo:hi], ref[lo:hi]))
+                if bad.size:
+                    return nm, lo + int(bad[0])
+            return None
+
+        for res in pool.map(cmp, slices):
+            if res is not None:
+                nm, j = res
+                i = "pmv".index(nm)
+                raise AssertionError(f"after {w.steps} steps {t.name} {nm}: element {j} got {final[k][i][j]!r} "
+                                     f"oracle {state[i][j]!r}")
+        checked += t.numel
+        final[k] = None
+        del state
+    assert checked == w.trainable_numel
+    pool.shutdown()
 
 
 def test_full_size_graph_replays():
