@@ -216,10 +216,11 @@ def _code_only(text):
 
 
 def kernel_source_hash():
-    """Hash of the kernels' code (comments and layout ignored): the ncu
-    traffic record applies only to the code it was measured on."""
+    """Hash of the kernels' code and of the host code that cuts the lists
+    into chunks (comments and layout ignored): the ncu traffic record applies
+    only to the code and launch shapes it was measured on."""
     h = hashlib.sha256()
-    for f in ("kernels.cu", "soma_kernels.h"):
+    for f in ("kernels.cu", "soma_kernels.h", "soma_opt.cpp"):
         with open(os.path.join(ROOT, "tensor_grad_clip_gb300", "csrc", f), encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]

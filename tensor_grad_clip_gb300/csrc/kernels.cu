@@ -628,7 +628,8 @@ __device__ __forceinline__ void store8(const Seg& s, int i, const Lane8& x) {
 }
 
 // L2 prefetch of the gradient, p, m and v of this thread's first
-// kPrefetchVectors vectors (half of a 16 Ki-element chunk).  Same-box sweep
+// kPrefetchVectors vectors (all of an 8 Ki-element chunk, two thirds of a
+// 12 Ki one; the sweep was taken with 16 Ki chunks).  Same-box sweep
 // of 0-8: 4 was best on every list (the step 0.7 % faster than with 2 on the
 // action-expert list, 0.6 % on the 7B shard view); 8 was up to 10 % slower.
 constexpr int kPrefetchVectors = 4;
