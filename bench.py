@@ -46,7 +46,9 @@ UNIT = "param-elements/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 DEFAULT_WORKLOAD = "hsdp_shard"
-DEFAULT_PER_CONFIG = "action_expert,flat,many_small,tiny"
+# list[:mode]: master = bf16 model weights rewritten from fp32 master weights
+# in the same pass; graph = one captured step (soma_opt_step_graph) replayed
+DEFAULT_PER_CONFIG = "action_expert,flat,many_small,tiny,action_expert:master,many_small:graph,tiny:graph"
 PER_CONFIG_MIN_S = 0.5   # timed seconds per per-config list, at least
 
 
@@ -749,13 +751,23 @@ def run_ours(args):
     if names is None:
         names = DEFAULT_PER_CONFIG if (args.workload == DEFAULT_WORKLOAD and not args.blocks) else "none"
     for name in [x for x in names.split(",") if x and x != "none" and x != args.workload]:
-        wk = workload(name)
+        base, _, mode = name.partition(":")
+        if mode not in ("", "master", "graph"):
+            raise SystemExit(f"unknown mode {mode!r} in --per-config {name}")
+        graph_k = mode == "graph" and world == 1  # (graph-capturable steps have no multi-rank form)
+        wk = workload(base, master=mode == "master")
         Sk = Setup(args, wk, local, rank, world)
-        probe = measure(args, Sk, stream, world, max(3, args.warmup), max(3, args.warmup), False, 0)
+        probe = measure(args, Sk, stream, world, max(3, args.warmup), max(3, args.warmup), graph_k, 0)
         est_ms = probe["elapsed_ms"] / probe["steps"]
         k = max(args.steps, min(20000, int(PER_CONFIG_MIN_S * 1e3 / max(est_ms, 1e-3)) + 1))
-        rk = measure(args, Sk, stream, world, k, 0, False, min(k, 300))
-        per[name] = {"config": describe(wk)} | summarize(wk, rk, world, hbm_peak)
+        rk = measure(args, Sk, stream, world, k, 0, graph_k, min(k, 300))
+        ent = summarize(wk, rk, world, hbm_peak)
+        if graph_k:  # a graph replay has no per-kernel events: drop the kernel fields
+            for f in ("update_kernel_ms", "norm_kernel_ms", "update_kernel_gbs", "norm_kernel_gbs"):
+                ent[f] = None
+        ent["mode"] = ("CUDA-graph replay of one step" if graph_k else "soma_opt_step per step") + \
+            (", bf16 model copies of fp32 master weights" if mode == "master" else "")
+        per[name] = {"config": describe(wk)} | ent
         Sk.close()
         del Sk
 

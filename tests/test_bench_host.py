@@ -58,4 +58,6 @@ def test_default_line_is_the_largest_single_gpu_list():
     assert bench.DEFAULT_WORKLOAD == "hsdp_shard"
     sizes = {k: f().trainable_numel for k, f in W.FULL.items()}
     assert max(sizes, key=sizes.get) == "hsdp_shard"
-    assert set(bench.DEFAULT_PER_CONFIG.split(",")) == set(W.FULL) - {"hsdp_shard"}
+    names = bench.DEFAULT_PER_CONFIG.split(",")
+    assert {x.partition(":")[0] for x in names} == set(W.FULL) - {"hsdp_shard"}
+    assert {x.partition(":")[2] for x in names} <= {"", "master", "graph"}
