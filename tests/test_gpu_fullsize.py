@@ -51,14 +51,21 @@ def _built():
     oracle.lib()
 
 
-def oracle_norm(w, host_g, divisor, pool):
-    """sqrt of the oracle's sum of (g/d)^2 over owned tensors; large tensors
-    are summed in pieces of 2^26 elements, pieces added in list order."""
+def divisor_of(w, k):
+    """Tensor k's effective-batch divisor: its group's own, else the list's."""
+    return w.groups[w.tensors[k].group].divisor or w.grad_divisor
+
+
+def oracle_norm(w, host_g, pool):
+    """sqrt of the oracle's sum of (g/d)^2 over owned tensors, d each
+    tensor's divisor; large tensors are summed in pieces of 2^26 elements,
+    pieces added in list order."""
     piece = 1 << 26
     tasks = [(k, a) for k, t in enumerate(w.tensors) if t.trainable and t.owned
              for a in range(0, t.numel, piece)]
     total = 0.0
-    for x in pool.map(lambda ka: oracle.tensor_sqsum(host_g[ka[0]][ka[1]:ka[1] + piece], divisor), tasks):
+    for x in pool.map(lambda ka: oracle.tensor_sqsum(host_g[ka[0]][ka[1]:ka[1] + piece], divisor_of(w, ka[0])),
+                      tasks):
         total += x
     return math.sqrt(total)
 
@@ -117,15 +124,18 @@ def run_full(w, steps, select=None, graph=False, extra_idx=None):
     dev = torch.device("cuda", 0)
     fb = W.FlatBuffers(w, dev, grad_step=1)
     opt = SomaOpt(0)
-    for q in w.groups:
+    for i, q in enumerate(w.groups):
         opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+        if q.divisor:
+            opt.set_group_divisor(i, q.divisor)
     tl = TensorList(fb.p, fb.g, fb.m, fb.v, groups=[t.group for t in w.tensors],
-                    trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
+                    trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors],
+                    params_lowp=fb.plow)
     p0 = [x.cpu() for x in fb.p]  # initial weights: fp32, converted to fp64 per checked element
     pool = ThreadPoolExecutor(POOL)
     stream = torch.cuda.Stream() if graph else None
     cuda_graph = torch.cuda.CUDAGraph() if graph else None
-    gbits = torch.int16 if fb.grad_dtype == torch.bfloat16 else torch.int32
+    gbits = torch.int16 if fb.G.element_size() == 2 else torch.int32
     idx = idx_t = state = host = None
     checked = 0
     for s in range(1, steps + 1):
@@ -152,7 +162,7 @@ def run_full(w, steps, select=None, graph=False, extra_idx=None):
         else:
             opt.step(tl, w.grad_divisor, w.max_norm)
             norm, coef, nonfinite = opt.get_norm()
-        rn = oracle_norm(w, host_g, w.grad_divisor, pool)
+        rn = oracle_norm(w, host_g, pool)
         rc = oracle.clip_coef(rn, w.max_norm)
         assert not nonfinite
         assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (s, norm, rn)
@@ -161,6 +171,9 @@ def run_full(w, steps, select=None, graph=False, extra_idx=None):
             assert coef == 1.0
         assert torch.equal(fb.G.view(gbits), g_before), "gradients changed"
         del g_before
+        for k, low in enumerate(fb.plow):  # 16-bit model copies: the round-to-nearest-even of the GPU's master
+            if low is not None:
+                assert torch.equal(low.view(torch.int16), fb.p[k].to(low.dtype).view(torch.int16)), (s, k)
 
         if idx is None:  # after the first step: choose the checked elements, seed their fp64 state
             sel = select(opt, fb) if select is not None else [None] * len(w.tensors)
@@ -195,7 +208,7 @@ def run_full(w, steps, select=None, graph=False, extra_idx=None):
             q = w.groups[t.group]
             p_s, m_s, v_s = (x[lo:hi] for x in state[k])
             oracle.adamw_update(p_s, gk[lo:hi], m_s, v_s, lr=lrs[t.group], beta1=q.beta1, beta2=q.beta2, eps=q.eps,
-                                weight_decay=q.weight_decay, step=s, c=rc, divisor=w.grad_divisor)
+                                weight_decay=q.weight_decay, step=s, c=rc, divisor=divisor_of(w, k))
             out = []
             for nm, got, ref in zip("pmv", host[k], (p_s, m_s, v_s)):
                 bad = _bad(got[lo:hi].numpy(), ref)
@@ -248,6 +261,24 @@ def test_full_size_every_element(name):
     assert plan["owned_numel"] == w.owned_numel
 
 
+def test_full_size_fp16_grads_master_copies_group_divisor():
+    # The action-expert list at full size with fp16 gradients, bf16 model
+    # copies rewritten from the fp32 master weights in the same pass, and the
+    # norm-weight group on its own effective-batch divisor (16 against the
+    # list's 64): the kernels' group-divisor variants and the large-list norm
+    # table that starts a chunk at every group change.  Every element after
+    # each of 3 chained steps; each bf16 copy bit for bit the rounding of the
+    # GPU's own master weights.
+    import dataclasses
+    w = W.action_expert(master=True, steps=3)
+    w = dataclasses.replace(
+        w, name=w.name + "-f16-groupdiv",
+        tensors=tuple(dataclasses.replace(t, grad_dtype=W.F16) for t in w.tensors),
+        groups=(w.groups[0], dataclasses.replace(w.groups[1], divisor=16.0)))
+    plan, checked = run_full(w, steps=3)
+    assert checked == w.trainable_numel
+
+
 def test_full_size_hsdp_shard_blocks_and_every_chunk_boundary():
     w = W.FULL["hsdp_shard"]()
     per_block = 8
@@ -289,7 +320,7 @@ def test_full_size_hsdp_shard_first_step_every_element():
     opt.step(tl, w.grad_divisor, w.max_norm)
     norm, coef, nonfinite = opt.get_norm()
     pool = ThreadPoolExecutor(POOL)
-    rn = oracle_norm(w, host_g, w.grad_divisor, pool)
+    rn = oracle_norm(w, host_g, pool)
     rc = oracle.clip_coef(rn, w.max_norm)
     assert not nonfinite
     assert math.isclose(norm, rn, rel_tol=NORM_RTOL), (norm, rn)
@@ -304,7 +335,7 @@ def test_full_size_hsdp_shard_first_step_every_element():
             p_s = p0[k].numpy()[lo:hi].astype(np.float64)
             m_s, v_s = np.zeros_like(p_s), np.zeros_like(p_s)
             oracle.adamw_update(p_s, host_g[k][lo:hi], m_s, v_s, lr=lrs[t.group], beta1=q.beta1, beta2=q.beta2,
-                                eps=q.eps, weight_decay=q.weight_decay, step=1, c=rc, divisor=w.grad_divisor)
+                                eps=q.eps, weight_decay=q.weight_decay, step=1, c=rc, divisor=divisor_of(w, k))
             out = []
             for nm, g_, r_ in zip("pmv", got, (p_s, m_s, v_s)):
                 bad = np.flatnonzero(_bad(g_[lo:hi], r_))
@@ -356,7 +387,7 @@ def test_full_size_hsdp_shard_ten_steps_every_element():
         opt.step(tl, w.grad_divisor, w.max_norm)
         norm, coef, nonfinite = opt.get_norm()
         host_g = [x.cpu() for x in fb.g]
-        rn = oracle_norm(w, host_g, w.grad_divisor, pool)
+        rn = oracle_norm(w, host_g, pool)
         del host_g
         rc = oracle.clip_coef(rn, w.max_norm)
         assert not nonfinite
@@ -386,7 +417,7 @@ def test_full_size_hsdp_shard_ten_steps_every_element():
                 hi = min(n, lo + SLICE)
                 oracle.adamw_update(state[0][lo:hi], g[lo:hi], state[1][lo:hi], state[2][lo:hi], lr=lr,
                                     beta1=q.beta1, beta2=q.beta2, eps=q.eps, weight_decay=q.weight_decay, step=s_,
-                                    c=coefs[s_ - 1], divisor=w.grad_divisor)
+                                    c=coefs[s_ - 1], divisor=divisor_of(w, k))
             list(pool.map(upd, slices))
             del g
 

@@ -36,7 +36,7 @@ class FlatBuffers:
         self.V = torch.empty(total, dtype=torch.float32, device=self.device)
         for buf in (self.P, self.M, self.V):
             buf.view(torch.int32).fill_(SENTINEL_F32)
-        if self.grad_dtype == torch.bfloat16:
+        if self.G.element_size() == 2:  # bf16 or fp16: 0x7FAD is a NaN in both
             self.G.view(torch.int16).fill_(SENTINEL_BF16)
         else:
             self.G.view(torch.int32).fill_(SENTINEL_F32)
@@ -76,8 +76,9 @@ class FlatBuffers:
         return out
 
     def gaps_intact(self) -> bool:
-        gsent = SENTINEL_BF16 if self.grad_dtype == torch.bfloat16 else SENTINEL_F32
-        gi = self.G.view(torch.int16 if self.grad_dtype == torch.bfloat16 else torch.int32)
+        half = self.G.element_size() == 2
+        gsent = SENTINEL_BF16 if half else SENTINEL_F32
+        gi = self.G.view(torch.int16 if half else torch.int32)
         for a, b in self.gaps():
             for buf in (self.P, self.M, self.V):
                 if not bool((buf.view(torch.int32)[a:b] == SENTINEL_F32).all()):
