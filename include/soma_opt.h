@@ -328,12 +328,16 @@ soma_status_t soma_opt_get_cache_stats(soma_opt_t opt, int64_t *builds, int64_t 
                                        int32_t *entries);
 
 /* Tuning knobs for benchmarks: elements per update chunk and per norm chunk
- * (rounded to a multiple of 64; 0 = automatic: update chunks of 12 Ki
- * elements, or 8 Ki when at least half of the trainable elements have fp32
- * gradients; norm chunks of 112 Ki, or 320 Ki with a shrinking tail for lists
- * whose owned tensors average at least 320 Ki elements; both less for lists
- * too small to give every SM four chunks, never below 1 Ki) and, per kernel,
- * resident CTAs per SM for a persistent grid (0 = one CTA per chunk).
+ * (rounded to a multiple of 64; 0 = automatic) and, per kernel, resident CTAs
+ * per SM for a persistent grid (0 = one CTA per chunk).  Automatic sizes:
+ *   update chunks of 12 Ki elements, or 8 Ki when at least half of the
+ *   trainable elements have fp32 gradients; a list that one wave of the
+ *   update kernel's resident CTAs (two per SM) holds in such chunks is cut
+ *   into one wave's worth instead, one that two waves hold into two waves'
+ *   worth, never below 1 Ki;
+ *   norm chunks of 112 Ki, or 320 Ki with a shrinking tail for lists whose
+ *   owned tensors average at least 320 Ki elements, and for lists too small
+ *   to give every SM four chunks, four per SM, never below 1 Ki.
  * Results do not depend on the grid, only on the chunk sizes.  Takes effect
  * at the next list (re)build. */
 soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t norm_chunk,

@@ -48,6 +48,7 @@ constexpr double kTailShare = 0.5;
 constexpr int64_t kTailFloor = 32768;
 constexpr int64_t kNormCtasPerSm = 3;  // the square-sum kernel's resident CTAs per SM
 constexpr int64_t kMinAutoChunk = 1024;   // smallest chunk the automatic sizing picks
+constexpr int64_t kUpdateCtasPerSm = 2;   // the update kernel's resident CTAs per SM (its launch bounds)
 constexpr int64_t kAutoChunksPerSm = 4;   // small lists: aim for this many chunks per SM
 constexpr int64_t kSinglePerCta = 4096;   // default single-launch limit: one 8-element vector per thread of each cluster CTA
 constexpr size_t kTimingRing = 1024;
@@ -339,6 +340,24 @@ int64_t chunk_size(int32_t requested, int32_t dflt, int64_t total, int sm_count)
     return std::max<int64_t>(kMinAutoChunk, std::min<int64_t>(dflt, spread));
 }
 
+// Elements per update chunk.  A list that one wave of the update kernel's
+// resident CTAs holds in default chunks is cut into exactly one wave's worth
+// of chunks: such lists are latency-bound, and each extra wave adds a CTA's
+// fixed cost (tables, the wait for the norm).  Same-box probe, lists of four
+// equal tensors, against two waves: 524 Ki elements 10.7 us from 12.4, 1 Mi
+// 13.3 from 14.3, 2 Mi 14.7 from 17.5, 3 Mi 18.4 from 19.7 (fp32 gradients
+// alike); 256 Ki and smaller unchanged (the 1 Ki floor).  Larger lists keep
+// chunk_size's rule.
+int64_t update_chunk_size(int32_t requested, int32_t dflt, int64_t total, int sm_count) {
+    if (requested > 0) return requested;
+    const int64_t slots = kUpdateCtasPerSm * std::max(sm_count, 1);
+    if (total <= slots * dflt) {
+        const int64_t one_wave = (total + slots - 1) / slots;
+        return std::max<int64_t>(kMinAutoChunk, (one_wave + 63) / 64 * 64);
+    }
+    return chunk_size(requested, dflt, total, sm_count);
+}
+
 // Makes plan i the one the next launches use.
 void activate(soma_opt* o, int i) {
     PreparedList& pl = o->plans[i];
@@ -386,12 +405,12 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
         const int64_t k = std::max(o->single_ctas, 1);
         return std::max<int64_t>(64, ((total + k - 1) / k + 63) / 64 * 64);
     };
-    TableBuilder upd(o->update_chunk == 0 && single ? per_cta(trainable_total)
-                                                    : chunk_size(o->update_chunk,
-                                                                 2 * f32_total >= trainable_total && trainable_total > 0
-                                                                     ? kDefaultUpdateChunkF32
-                                                                     : kDefaultUpdateChunk,
-                                                                 trainable_total, o->sm_count), false);
+    const int32_t upd_default =
+        trainable_total > 0 && 2 * f32_total >= trainable_total ? kDefaultUpdateChunkF32 : kDefaultUpdateChunk;
+    TableBuilder upd(o->update_chunk == 0 && single
+                         ? per_cta(trainable_total)
+                         : update_chunk_size(o->update_chunk, upd_default, trainable_total, o->sm_count),
+                     false);
     const bool large = o->norm_chunk == 0 && !single && owned_tensors > 0 &&
                        owned_total / owned_tensors >= kLargeNormChunk;
     TableBuilder nrm(o->norm_chunk == 0 && single ? per_cta(owned_total)
