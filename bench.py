@@ -480,6 +480,9 @@ def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
             "mode": "pipelined: two device gradient buffers, upload of step t+1 overlaps step t; "
                     "median of three windows",
             "h2d_link_gbs": link_gbs,
+            # the upload alone at the link rate measured above: no step can be faster
+            "link_floor_ms": G.numel() * G.element_size() / (link_gbs * 1e9) * 1e3,
+            "frac_of_link_floor": (G.numel() * G.element_size() / (link_gbs * 1e9) * 1e3) / p_ms,
             "serial": {"value": elems / (s_ms / 1e3), "ms_per_step": s_ms, "windows_ms_per_step": s_all}}
 
 
