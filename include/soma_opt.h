@@ -405,14 +405,16 @@ void soma_opt_destroy(soma_opt_t opt);
  * least 26 000 owned entries fit whatever their sizes (about 65 000 when they
  * are small enough to share chunks).
  *
- * Blocking: each call copies the tables from a host buffer that the next call
- * rewrites, and waits for `stream` after that copy, so it returns only once
- * all work enqueued earlier on `stream` (the caller's backward pass, say) has
- * finished; the kernel and the copy to `out` then stay queued.  The first
- * call on a device, with that device made current, also looks up the array's
- * device address and keeps it; make that first call before any stream
- * capture.  Every call shares the array and overwrites what the previous call
- * left there (it clears the result block each time).  Calls that overlap on
+ * Asynchrony: the call enqueues its work on `stream` and returns without
+ * waiting for the GPU.  The tables travel to the array in the arguments of
+ * small copy kernels (one launch per 30,400 bytes of table; a launch copies
+ * its arguments when it is enqueued), then the square-sum kernel and a
+ * device-to-device copy of {norm, c} to `out` follow, so `out` is valid once
+ * `stream` reaches that point.  The first call on a device, with that device
+ * made current, also looks up the array's device address and keeps it; make
+ * that first call before any stream capture.  Every call shares the array
+ * and overwrites what the previous call left there (it clears the result
+ * block each time).  Calls on one stream are ordered; calls that overlap on
  * the GPU -- on unordered streams, or from several host threads -- race on
  * the array: order them.  Returns SOMA_ERR_INVALID_ARG, SOMA_ERR_DTYPE,
  * SOMA_ERR_ALIGNMENT, SOMA_ERR_LIMIT or SOMA_ERR_CUDA (no detail text). */

@@ -18,9 +18,10 @@
 // name is only a host-side stand-in, not a device address) and caches it.
 // Make that first call before any stream capture.
 //
-// Each call waits for its stream after copying the tables (see the copy
-// below), so it returns only once everything enqueued earlier on that stream
-// has finished.
+// The tables reach the array inside the arguments of small copy kernels:
+// a launch copies its arguments when it is enqueued, so the host staging
+// buffer is free again as soon as the launches are enqueued, and a call
+// returns without waiting for anything on the GPU.
 //
 // All calls share the one array, which keeps the contents of the last call:
 // every call rewrites the tables and clears the result/ticket block before
@@ -44,6 +45,23 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kResultBytes = 256;         // soma::Result, padded
 constexpr int64_t kMinChunk = 32768;          // elements per chunk, at least
 constexpr int64_t kTargetChunks = 32768;      // grows the chunk for large lists
+// 16-byte words of the staged image one copy launch carries in its
+// arguments (30,400 bytes; kernel arguments may take up to 32,764).
+constexpr int kArgWords = 1900;
+
+// Arguments of one copy launch: `nwords` words for `dst` (16-byte aligned).
+struct StageArgs {
+    uint4* dst;
+    int32_t nwords;
+    int32_t pad;
+    uint4 words[kArgWords];
+};
+static_assert(sizeof(StageArgs) <= 32764, "kernel arguments are limited to 32,764 bytes");
+
+__global__ void write_stage_kernel(const __grid_constant__ StageArgs a) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.nwords; i += gridDim.x * blockDim.x)
+        a.dst[i] = a.words[i];
+}
 
 }  // namespace
 
@@ -53,6 +71,7 @@ namespace {
 
 std::mutex g_mu;                               // one host-side user at a time
 alignas(256) unsigned char g_stage[kScratchBytes];  // host image of the scratch
+StageArgs g_args;                              // arguments of the copy launch being enqueued
 void* g_dev_scratch[kMaxDevices];              // per device: address of the array
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -169,13 +188,20 @@ extern "C" soma_status_t soma_clip_norm_noalloc(int32_t device, const soma_tenso
     norm_table(list, n, chunk, reinterpret_cast<soma::Seg*>(g_stage + o_seg),
                reinterpret_cast<int32_t*>(g_stage + o_beg), &nseg, &nchunk);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The copy may read g_stage only when it runs on the stream (the GPU can
-    // read pageable host memory directly on this platform), so wait for it
-    // before returning: the next call rewrites g_stage.
-    if (cudaMemcpyAsync(d, g_stage, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess) {
-        cudaGetLastError();
-        return SOMA_ERR_CUDA;
+    // The result block (cleared) and the tables go to the array in the
+    // arguments of copy launches, whose arguments are copied at enqueue time:
+    // g_stage may be rewritten by the next call as soon as this one returns.
+    // The partial sums need no copy; the square-sum kernel writes them.
+    const size_t regions[2][2] = {{0, kResultBytes}, {o_seg, bytes}};
+    for (const auto& rg : regions) {
+        for (size_t off = rg[0]; off < rg[1]; off += sizeof(g_args.words)) {
+            const size_t n16 = (std::min(rg[1] - off, sizeof(g_args.words)) + 15) / 16;
+            g_args.dst = reinterpret_cast<uint4*>(d + off);
+            g_args.nwords = (int32_t)n16;
+            std::memcpy(g_args.words, g_stage + off, n16 * 16);
+            write_stage_kernel<<<(int)std::min<size_t>(8, (n16 + 255) / 256), 256, 0, s>>>(g_args);
+            if (cudaGetLastError() != cudaSuccess) return SOMA_ERR_CUDA;
+        }
     }
     soma::NormArgs a{};
     a.t = soma::Table{reinterpret_cast<const soma::Seg*>(d + o_seg), reinterpret_cast<const int32_t*>(d + o_beg),

@@ -19,6 +19,7 @@ first failure has run every other test before this one.
 import ctypes
 import dataclasses
 import math
+import time
 
 import pytest
 import torch
@@ -89,6 +90,36 @@ def test_calls_in_a_row_match_the_oracle_and_the_step():
         opt.close()
         assert math.isclose(got_norm, norm, rel_tol=NORM_RTOL), (w.name, got_norm, norm)
         assert math.isclose(got_coef, coef, rel_tol=NORM_RTOL), (w.name, got_coef, coef)
+
+
+def test_call_returns_without_waiting_for_the_gpu():
+    # A caller in a latency-critical loop enqueues the norm behind work that
+    # is still running on the stream (here a timed 0.3 s spin).  The call
+    # returns at once (its tables travel in kernel arguments, not through a
+    # host buffer that has to outlive the call), and the result is right once
+    # the stream gets there.
+    w = W.with_steps(W.SMALL["action_expert"](), 1)
+    params = W.draw_params(w, "cpu")
+    grads = W.draw_grads(w, 1, "cpu")
+    dl = DeviceList(w, params)
+    dl.load_grads(grads)
+    out = torch.full((2,), float("nan"), dtype=torch.float64, device="cuda")
+    assert _noalloc(dl.tl, w.grad_divisor, w.max_norm, out) == _abi.SOMA_OK  # first call: set-up
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    torch.cuda._sleep(600_000_000)  # 600 M cycles: about 0.3 s at the SM clock
+    t0 = time.perf_counter()
+    st = _noalloc(dl.tl, w.grad_divisor, w.max_norm, out)
+    dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    t_all = time.perf_counter() - t0
+    assert st == _abi.SOMA_OK
+    assert t_all > 0.1, t_all  # the spin really ran ahead of the norm on the stream
+    assert dt < 0.5 * t_all, (dt, t_all)
+    got_norm, got_coef = out.cpu().tolist()
+    rn = make_oracle(w, params).global_norm(grads, w.grad_divisor)
+    assert math.isclose(got_norm, rn, rel_tol=NORM_RTOL), (got_norm, rn)
+    assert math.isclose(got_coef, oracle.clip_coef(rn, w.max_norm), rel_tol=NORM_RTOL)
 
 
 def test_oversized_list_is_refused_before_any_work():
