@@ -335,9 +335,10 @@ soma_status_t soma_opt_get_cache_stats(soma_opt_t opt, int64_t *builds, int64_t 
  *   update kernel's resident CTAs (two per SM) holds in such chunks is cut
  *   into one wave's worth instead, one that two waves hold into two waves'
  *   worth, never below 1 Ki;
- *   norm chunks of 112 Ki, or 320 Ki with a shrinking tail for lists whose
- *   owned tensors average at least 320 Ki elements, and for lists too small
- *   to give every SM four chunks, four per SM, never below 1 Ki.
+ *   norm chunks of 320 Ki with a shrinking tail for lists whose owned
+ *   tensors average at least 320 Ki elements; for other lists 112 Ki, or one
+ *   wave of the square-sum kernel's resident CTAs (three per SM) for a list
+ *   that one wave holds in such chunks, never below 1 Ki.
  * Results do not depend on the grid, only on the chunk sizes.  Takes effect
  * at the next list (re)build. */
 soma_status_t soma_opt_set_tuning(soma_opt_t opt, int32_t update_chunk, int32_t norm_chunk,

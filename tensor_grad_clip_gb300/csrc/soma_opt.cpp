@@ -358,6 +358,22 @@ int64_t update_chunk_size(int32_t requested, int32_t dflt, int64_t total, int sm
     return chunk_size(requested, dflt, total, sm_count);
 }
 
+// Elements per norm chunk of a list whose owned tensors are small on
+// average (large ones take kLargeNormChunk): a list that one wave of the
+// square-sum kernel's resident CTAs holds in default chunks is cut into one
+// wave's worth.  Same-box probe against four chunks per SM: lists of 200,
+// 700, 2 700 and 8 000 small tensors (0.7-44 M elements) 3.5-12 % faster
+// steps, 1 Mi elements in four tensors 5 %; 256 Ki and smaller unchanged.
+int64_t norm_chunk_size(int32_t requested, int32_t dflt, int64_t owned, int sm_count) {
+    if (requested > 0) return requested;
+    const int64_t slots = kNormCtasPerSm * std::max(sm_count, 1);
+    if (owned <= slots * dflt) {
+        const int64_t one_wave = (owned + slots - 1) / slots;
+        return std::max<int64_t>(kMinAutoChunk, (one_wave + 63) / 64 * 64);
+    }
+    return chunk_size(requested, dflt, owned, sm_count);
+}
+
 // Makes plan i the one the next launches use.
 void activate(soma_opt* o, int i) {
     PreparedList& pl = o->plans[i];
@@ -415,8 +431,8 @@ soma_status_t rebuild(soma_opt* o, const soma_tensor_t* list, int64_t n, void* s
                        owned_total / owned_tensors >= kLargeNormChunk;
     TableBuilder nrm(o->norm_chunk == 0 && single ? per_cta(owned_total)
                      : large                      ? kLargeNormChunk
-                                                  : chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total,
-                                                               o->sm_count), true);
+                                                  : norm_chunk_size(o->norm_chunk, kDefaultNormChunk, owned_total,
+                                                                    o->sm_count), true);
     if (large) {
         nrm.tail_total = owned_total;
         nrm.tail_slots = (int64_t)o->sm_count * kNormCtasPerSm;
