@@ -398,13 +398,13 @@ def test_full_size_hsdp_shard_ten_steps_every_element():
         assert opt.get_group_step(q) == w.steps
     torch.cuda.synchronize()
     assert fb.gaps_intact(), "a write landed outside a tensor"
-    final = [[x.cpu().numpy() for x in (fb.p[k], fb.m[k], fb.v[k])] for k in range(len(w.tensors))]
     opt.close()
-    del fb, tl
-    torch.cuda.empty_cache()
 
+    # each tensor's final state comes back only when it is checked, so the
+    # host holds one tensor's p, m, v at a time (the list's are 78 GB)
     checked = 0
     for k, t in enumerate(w.tensors):
+        final_k = [x.cpu().numpy() for x in (fb.p[k], fb.m[k], fb.v[k])]
         q = w.groups[t.group]
         state = [W.draw_param(w, k, dev).reshape(-1).cpu().numpy().astype(np.float64)]
         state += [np.zeros_like(state[0]), np.zeros_like(state[0])]
@@ -421,9 +421,9 @@ def test_full_size_hsdp_shard_ten_steps_every_element():
             list(pool.map(upd, slices))
             del g
 
-        def cmp(lo, k=k, state=state, n=t.numel):
+        def cmp(lo, final_k=final_k, state=state, n=t.numel):
             hi = min(n, lo + SLICE)
-            for nm, got, ref in zip("pmv", final[k], state):
+            for nm, got, ref in zip("pmv", final_k, state):
                 bad = np.flatnonzero(_bad(got[lo:hi], ref[lo:hi]))
                 if bad.size:
                     return nm, lo + int(bad[0])
@@ -433,13 +433,14 @@ def test_full_size_hsdp_shard_ten_steps_every_element():
             if res is not None:
                 nm, j = res
                 i = "pmv".index(nm)
-                raise AssertionError(f"after {w.steps} steps {t.name} {nm}: element {j} got {final[k][i][j]!r} "
+                raise AssertionError(f"after {w.steps} steps {t.name} {nm}: element {j} got {final_k[i][j]!r} "
                                      f"oracle {state[i][j]!r}")
         checked += t.numel
-        final[k] = None
-        del state
+        del state, final_k
     assert checked == w.trainable_numel
     pool.shutdown()
+    del fb, tl
+    torch.cuda.empty_cache()
 
 
 def test_full_size_graph_replays():
