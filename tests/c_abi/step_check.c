@@ -2,7 +2,9 @@
  * step through the C ABI, the result checked on the host against the
  * first-step closed form of AdamW.  With m = v = 0 before step 1,
  * m_hat = g' and v_hat = g'^2, so p1 = p0 (1 - lr wd) - lr g' / (|g'| + eps)
- * with g' = c g / d.  Exit status 0 on success. */
+ * with g' = c g / d.  Then the allocation-free norm of the same gradients
+ * (which the step left unchanged) against the same norm and c.  Exit status
+ * 0 on success. */
 #include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -59,6 +61,18 @@ int main(void) {
             return 1;
         }
     }
+    /* the norm and c again, from the entry point that allocates nothing */
+    double *dnc = NULL, hnc[2] = {0.0, 0.0};
+    if (cudaMalloc((void **)&dnc, sizeof hnc) || soma_clip_norm_noalloc(0, &t, 1, d, max_norm, dnc, NULL) ||
+        cudaMemcpy(hnc, dnc, sizeof hnc, cudaMemcpyDeviceToHost)) {
+        fprintf(stderr, "no-alloc norm failed\n");
+        return 1;
+    }
+    if (fabs(hnc[0] - ref_norm) > 1e-5 * ref_norm || fabs(hnc[1] - ref_c) > 1e-5 * ref_c) {
+        fprintf(stderr, "no-alloc norm %.9g (ref %.9g), c %.9g (ref %.9g)\n", hnc[0], ref_norm, hnc[1], ref_c);
+        return 1;
+    }
+    cudaFree(dnc);
     soma_opt_destroy(opt);
     cudaFree(p);
     cudaFree(g);

@@ -42,7 +42,8 @@ def test_header_links_from_cpp(tmp_path):
 @pytest.mark.gpu
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
 def test_c99_program_runs_a_step(tmp_path):
-    # No Python on the path: CUDA runtime buffers, one step, the closed form.
+    # No Python on the path: CUDA runtime buffers, one step, the closed form,
+    # and the allocation-free norm of the same gradients.
     lib = build.build()
     cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
     exe = tmp_path / "step_check"
