@@ -432,10 +432,16 @@ def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
                 upload(t + 1)
             opt.get_norm(stream)
 
+    upload_ms = []  # each upload of the serial mode, from events on the copy stream
+
     def serial(n):
         for _ in range(n):
             cs.wait_stream(stream)
+            u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            u0.record(cs)
             upload(0)
+            u1.record(cs)  # right behind the copy on the copy stream
+            upload_ms.append((u0, u1))
             stream.wait_event(copied[0])
             opt = step_on(tl)
             freed[0].record(stream)
@@ -474,6 +480,8 @@ def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
     p_all = [timed(pipelined, n) / n for _ in range(3)]
     s_all = [timed(serial, n) / n for _ in range(3)]
     p_ms, s_ms = statistics.median(p_all), statistics.median(s_all)
+    torch.cuda.synchronize()
+    up_ms = statistics.median(a.elapsed_time(b) for a, b in upload_ms[-n:])
     return {"value": elems / (p_ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": 48,
             "steps": n, "ms_per_step": p_ms, "windows_ms_per_step": p_all,
@@ -483,7 +491,9 @@ def e2e_runs(args, w, fb, tl, owned, step_on, stream, device, barrier, world):
             # the upload alone at the link rate measured above: no step can be faster
             "link_floor_ms": G.numel() * G.element_size() / (link_gbs * 1e9) * 1e3,
             "frac_of_link_floor": (G.numel() * G.element_size() / (link_gbs * 1e9) * 1e3) / p_ms,
-            "serial": {"value": elems / (s_ms / 1e3), "ms_per_step": s_ms, "windows_ms_per_step": s_all}}
+            "serial": {"value": elems / (s_ms / 1e3), "ms_per_step": s_ms, "windows_ms_per_step": s_all,
+                       # the upload alone inside the serial loop, against the link test above
+                       "upload_ms_median": up_ms, "upload_gbs": G.numel() * G.element_size() / (up_ms * 1e6)}}
 
 
 def kernel_bytes(w):
