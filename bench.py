@@ -20,8 +20,10 @@ roofline entry for the update kernel, the oracle's CPU throughput, an
 end-to-end number through the C ABI with host-resident gradients, and the SM
 clocks seen during the timed region.  `per_config` holds the same
 device-side measurement for the other lists (by default the action-expert,
-flat, 20 000-tensor and tiny lists), each set up after the previous list's
-buffers were freed, in the same process.
+flat, 20 000-tensor and tiny lists, the action-expert list with bf16 model
+copies of fp32 master weights, and graph replays of the 20 000-tensor and
+tiny lists), each set up after the previous list's buffers were freed, in
+the same process.
 
 --impl reference times the fp64 CPU oracle (the only other implementation of
 this step available here) on bounded samples of the same workload.
