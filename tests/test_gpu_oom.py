@@ -70,3 +70,23 @@ def test_table_allocation_failure_returns_oom_and_changes_nothing():
     assert not nonfinite and math.isclose(norm, ref, rel_tol=1e-5)
     assert opt.get_group_step(0) == steps_before + 1
     opt.close()
+
+
+def test_list_too_large_for_free_memory_is_refused_before_allocating(monkeypatch):
+    # The flat buffers of a list are checked against the free device memory
+    # before any allocation: a list larger than what is free raises
+    # MemoryError naming both figures, and nothing is allocated.
+    import workloads as W
+    from workloads import device as D
+    w = W.SMALL["action_expert"]()
+    allocated = torch.cuda.memory_allocated()
+    monkeypatch.setattr(D.torch.cuda, "mem_get_info", lambda device=None: (1 << 20, 1 << 40))
+    monkeypatch.setattr(D.torch.cuda, "memory_reserved", lambda device=None: allocated)  # no cached blocks
+    with pytest.raises(MemoryError, match="GB are free"):
+        D.FlatBuffers(w, "cuda")
+    assert torch.cuda.memory_allocated() == allocated
+    monkeypatch.undo()
+    fb = D.FlatBuffers(w, "cuda")  # with the real figure it fits
+    assert fb.P.numel() >= w.trainable_numel
+    del fb
+    torch.cuda.empty_cache()

@@ -15,6 +15,26 @@ SENTINEL_BF16 = 0x7FAD
 ALIGN = 64                  # elements: 256 B of fp32, 128 B of bf16
 
 
+def bytes_per_slot(grad_dtype, lowp: bool) -> int:
+    """Device bytes per element slot of the flat buffers: fp32 weight, first
+    and second moment, the gradient, and a 16-bit model copy if any."""
+    return 12 + torch.empty((), dtype=grad_dtype).element_size() + (2 if lowp else 0)
+
+
+def check_device_memory(w: Workload, device, buffer_bytes: int):
+    """Refuses a list that does not fit before anything is allocated: the
+    flat buffers plus one tensor's draw (its fp32 values and their cast, 8
+    bytes per element of the largest tensor) against the free device memory,
+    counting what torch's caching allocator holds unused (it hands that out
+    again, or releases it, before an allocation fails)."""
+    need = buffer_bytes + 8 * max((t.numel for t in w.tensors), default=0)
+    free, _ = torch.cuda.mem_get_info(device)
+    free += torch.cuda.memory_reserved(device) - torch.cuda.memory_allocated(device)
+    if need > free:
+        raise MemoryError(f"{w.name} needs {need / 1e9:.2f} GB on {device} for its buffers and draws; "
+                          f"{free / 1e9:.2f} GB are free")
+
+
 class FlatBuffers:
     def __init__(self, w: Workload, device, grad_step: int = 1, gap: int = ALIGN, shard_rank: int = 0):
         self.w = w
@@ -30,6 +50,11 @@ class FlatBuffers:
         if len(gdts) != 1:
             raise ValueError("one gradient dtype per flat workload")
         self.grad_dtype = gdts.pop()
+        lows = {t.param_lowp for t in w.tensors if t.param_lowp}
+        if len(lows) > 1:
+            raise ValueError("one model-copy dtype per flat workload")
+        if self.device.type == "cuda":
+            check_device_memory(w, self.device, total * bytes_per_slot(self.grad_dtype, bool(lows)))
         self.P = torch.empty(total, dtype=torch.float32, device=self.device)
         self.G = torch.empty(total, dtype=self.grad_dtype, device=self.device)
         self.M = torch.empty(total, dtype=torch.float32, device=self.device)
@@ -40,9 +65,6 @@ class FlatBuffers:
             self.G.view(torch.int16).fill_(SENTINEL_BF16)
         else:
             self.G.view(torch.int32).fill_(SENTINEL_F32)
-        lows = {t.param_lowp for t in w.tensors if t.param_lowp}
-        if len(lows) > 1:
-            raise ValueError("one model-copy dtype per flat workload")
         self.PL = None
         if lows:
             self.PL = torch.empty(total, dtype=torch_dtype(lows.pop()), device=self.device)
