@@ -44,6 +44,10 @@ MISTAKES = [
      [("double dk = groups[ts[k].group].divisor > 0.0 ? groups[ts[k].group].divisor : divisor;",
        "double dk = divisor;")]),
     ("group divisor ignored in the update", [("gp->divisor > 0.0 ? gp->divisor : divisor);", "divisor);")]),
+    ("binary16 exponent bias off by one", [("ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)")]),
+    ("binary16 subnormals given the implicit bit", [("v = ldexp((double)f, -24);", "v = ldexp((double)(1024 + f), -25);")]),
+    ("binary16 sign dropped", [("return sign ? -v : v;", "return v;")]),
+    ("fp16 gradients decoded as bf16", [("if (dtype == ORACLE_GRAD_F16)\n", "if (0)\n")]),
 ]
 
 PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_golden.py"]
