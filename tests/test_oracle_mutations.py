@@ -48,6 +48,17 @@ MISTAKES = [
     ("binary16 subnormals given the implicit bit", [("v = ldexp((double)f, -24);", "v = ldexp((double)(1024 + f), -25);")]),
     ("binary16 sign dropped", [("return sign ? -v : v;", "return v;")]),
     ("fp16 gradients decoded as bf16", [("if (dtype == ORACLE_GRAD_F16)\n", "if (0)\n")]),
+    ("global norm without the square root", [("    return sqrt(total);", "    return total;")]),
+    ("step norm without the square root", [("double norm = sqrt(total);", "double norm = total;")]),
+    ("clip coefficient applied twice", [("/ divisor * c;", "/ divisor * c * c;")]),
+    ("update with the unclipped gradient", [("/ divisor * c;", "/ divisor;")]),
+    ("frozen tensors updated", [("        if (!ts[k].trainable)\n            continue;\n        const oracle_group",
+                                 "        const oracle_group")]),
+    ("replicated tensors not updated", [("        if (!ts[k].trainable)\n            continue;\n        const oracle_group",
+                                         "        if (!ts[k].trainable || !ts[k].owned)\n            continue;\n"
+                                         "        const oracle_group")]),
+    ("first bias correction multiplied", [("double m_hat = m[i] / bc1;", "double m_hat = m[i] * bc1;")]),
+    ("NaN norm clamped to 1", [("    if (isnan(c))\n        return c;\n", "")]),
 ]
 
 PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_golden.py"]
