@@ -299,6 +299,46 @@ def test_full_size_hsdp_shard_blocks_and_every_chunk_boundary():
     assert plan["owned_numel"] == w.owned_numel
 
 
+def test_full_size_hsdp_shard_run_to_run_bitwise_identical():
+    # The step is reproducible at full size: two runs of two chained steps
+    # from the same state, on two copies of the weights and moments at
+    # different addresses (same alignment), each through a fresh handle,
+    # give the same norms and the same p, m and v bit for bit.  The norm is
+    # the only reduction; its fixed-order sum of chunk partials does not
+    # depend on which CTA finishes last.
+    w = W.FULL["hsdp_shard"]()
+    dev = torch.device("cuda", 0)
+    fb = W.FlatBuffers(w, dev, grad_step=1)
+    P2, M2, V2 = fb.P.clone(), fb.M.clone(), fb.V.clone()  # the same initial state, 78 GB
+
+    def views(buf):
+        return [buf[fb.offsets[k]:fb.offsets[k] + t.numel] for k, t in enumerate(w.tensors)]
+
+    def run(p, m, v):
+        opt = SomaOpt(0)
+        for q in w.groups:
+            opt.add_group(lr=q.lr, betas=(q.beta1, q.beta2), eps=q.eps, weight_decay=q.weight_decay)
+        tl = TensorList(p, fb.g, m, v, groups=[t.group for t in w.tensors],
+                        trainable=[t.trainable for t in w.tensors], owned=[t.owned for t in w.tensors])
+        norms = []
+        for s in (1, 2):
+            fb.load_grads(s)
+            for q, lr in enumerate(w.group_lrs(s)):
+                opt.set_lr(q, lr)
+            opt.step(tl, w.grad_divisor, w.max_norm)
+            norms.append(opt.get_norm()[0])
+        opt.close()
+        return norms
+
+    a = run(fb.p, fb.m, fb.v)
+    b = run(views(P2), views(M2), views(V2))
+    torch.cuda.synchronize()
+    assert [x.hex() for x in a] == [x.hex() for x in b]
+    for x, y in ((fb.P, P2), (fb.M, M2), (fb.V, V2)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert fb.gaps_intact()
+
+
 def test_full_size_hsdp_shard_first_step_every_element():
     # Every element of the 7B shard view after its first step: the oracle
     # starts from the same seeded weights with zero moments, so each tensor

@@ -60,8 +60,9 @@ def _final_state(w, tuning=None, shift=None):
     return [torch.tensor(norms, dtype=torch.float64)] + [x.cpu().clone() for x in dl.p + dl.m + dl.v]
 
 
-def test_run_to_run_bitwise_identical():
-    w = W.with_steps(W.SMALL["many_small"](), 3)
+@pytest.mark.parametrize("name", ["tiny", "action_expert", "many_small", "hsdp_shard", "flat"])
+def test_run_to_run_bitwise_identical(name):
+    w = W.with_steps(W.SMALL[name](), 3)
     a = _final_state(w)
     b = _final_state(w)
     for x, y in zip(a, b):
