@@ -69,6 +69,54 @@ def test_run_to_run_bitwise_identical(name):
         assert torch.equal(x, y)
 
 
+def test_checkpoint_resume_bitwise_equal_to_an_uninterrupted_run():
+    # A checkpoint after step k holds the caller's weights and moments (its
+    # own buffers) and the handle's state_dict (group settings, divisors and
+    # step counts; bias corrections depend on the counts).  A fresh handle
+    # restored from it, on fresh buffers loaded from the checkpoint, runs the
+    # remaining steps: norms, weights and moments equal a run that never
+    # stopped, bit for bit.
+    import json
+    from dataclasses import replace
+    w = W.with_steps(W.SMALL["hsdp_shard"](), 6)  # two groups, replicated tensors
+    w = replace(w, groups=(replace(w.groups[0], divisor=3.0), w.groups[1]))  # one group on its own divisor
+    k = 3
+    whole = _final_state(w)
+    params = W.draw_params(w, "cpu")
+
+    def run(opt, dl, steps):
+        norms = []
+        for s in steps:
+            dl.load_grads(W.draw_grads(w, s, "cpu"))
+            for q, lr in enumerate(w.group_lrs(s)):
+                opt.set_lr(q, lr)
+            opt.step(dl.tl, w.grad_divisor, w.max_norm)
+            norms.append(opt.get_norm()[0])
+        return norms
+
+    dl = DeviceList(w, params)
+    opt = make_opt(w)
+    norms = run(opt, dl, range(1, k + 1))
+    torch.cuda.synchronize()
+    state = json.loads(json.dumps(opt.state_dict()))  # as a checkpoint file holds it
+    saved = [x.cpu().clone() for x in dl.p + dl.m + dl.v]
+    opt.close()
+    del dl
+    dl2 = DeviceList(w, params)  # new buffers, at other addresses
+    for dst, src in zip(dl2.p + dl2.m + dl2.v, saved):
+        dst.copy_(src)
+    opt2 = SomaOpt(0)
+    opt2.load_state_dict(state)
+    assert [opt2.get_group_step(q) for q in range(len(w.groups))] == [k] * len(w.groups)
+    norms += run(opt2, dl2, range(k + 1, w.steps + 1))
+    torch.cuda.synchronize()
+    resumed = [torch.tensor(norms, dtype=torch.float64)] + [x.cpu().clone() for x in dl2.p + dl2.m + dl2.v]
+    opt2.close()
+    for x, y in zip(whole, resumed):
+        assert torch.equal(x.view(torch.int64) if x.dtype == torch.float64 else x.view(torch.int32),
+                           y.view(torch.int64) if y.dtype == torch.float64 else y.view(torch.int32))
+
+
 @pytest.mark.parametrize("pattern", ["same_offset", "mixed_offset"])
 def test_unaligned_views(pattern):
     # same_offset: every buffer one element off the 16-byte grid (vector body
@@ -219,29 +267,6 @@ def test_side_stream_and_handoff_between_streams():
     for k in range(len(w.tensors)):
         assert_close("p", dl.p[k].cpu().numpy(), orc.params[k])
     opt.close()
-
-
-def test_checkpoint_resume_is_bitwise():
-    w = W.with_steps(W.SMALL["hsdp_shard"](), 4)
-    full = _final_state(w)
-    params = W.draw_params(w, "cpu")
-    dl = DeviceList(w, params)
-    opt = make_opt(w)
-    for s in (1, 2):
-        dl.load_grads(W.draw_grads(w, s, "cpu"))
-        opt.step(dl.tl, w.grad_divisor, w.max_norm)
-    steps = [opt.get_group_step(q) for q in range(len(w.groups))]
-    opt.close()  # "save": the caller owns p, m, v; the library state is the step counts
-    opt = make_opt(w)
-    for q, t in enumerate(steps):
-        opt.set_group_step(q, t)
-    for s in (3, 4):
-        dl.load_grads(W.draw_grads(w, s, "cpu"))
-        opt.step(dl.tl, w.grad_divisor, w.max_norm)
-    torch.cuda.synchronize()
-    opt.close()
-    for x, y in zip(full[1:], [t.cpu() for t in dl.p + dl.m + dl.v]):
-        assert torch.equal(x, y)
 
 
 def test_list_change_rebuilds_tables():
