@@ -140,6 +140,24 @@ class DeviceList:
                 raise AssertionError(f"frozen tensor {k}'s model copy changed")
 
 
+def sixty_four_groups(steps=3) -> W.Workload:
+    """A list at the group limit (SOMA_MAX_GROUPS = 64): tensor k in group k,
+    every group with its own lr, betas, eps and weight decay, every fifth on
+    its own divisor; fp32, bf16 and fp16 gradients in turn, some replicated
+    (not owned) and some frozen entries (their groups do not step).  59,168
+    trainable-or-frozen elements in all, small enough for the single-launch
+    step."""
+    T = W.TensorSpec
+    dts = (W.F32, W.BF16, W.F16)
+    tensors = tuple(T(f"t{k}", (200 + 23 * k,), dts[k % 3], group=k, owned=(k % 7 != 3),
+                      trainable=(k % 11 != 5)) for k in range(64))
+    groups = tuple(W.GroupSpec(lr=1e-3 * (1 + k / 64), beta1=0.8 + 0.003 * k, beta2=0.95 + 0.0007 * k,
+                               eps=1e-8 * (1 + k), weight_decay=0.002 * k,
+                               divisor=(2.0 + k % 3) if k % 5 == 0 else 0.0) for k in range(64))
+    return W.Workload(name="groups64", tensors=tensors, groups=groups, grad_divisor=2.0, max_norm=1.0,
+                      steps=steps, grad_std=1.0)
+
+
 def make_opt(w: W.Workload, device_index=0) -> SomaOpt:
     opt = SomaOpt(device_index)
     for q, g in enumerate(w.groups):

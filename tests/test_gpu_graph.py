@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from parity_harness import NORM_RTOL, DeviceList, assert_close, make_opt, make_oracle
+from parity_harness import NORM_RTOL, DeviceList, assert_close, make_opt, make_oracle, sixty_four_groups
 from tensor_grad_clip_gb300 import SomaError, TensorList, _abi, build
 
 pytestmark = pytest.mark.gpu
@@ -91,12 +91,25 @@ def test_graph_replays_equal_regular_steps_bit_for_bit(group_div):
     w = W.with_steps(W.SMALL["hsdp_shard"](), 4)  # two groups, bf16 grads, replicated tensors
     if group_div:
         w = replace(w, groups=(replace(w.groups[0], divisor=3.0), w.groups[1]))
-    resume = (123457, 7)
+    _regular_vs_graph(w, (123457, 7))
+
+
+@pytest.mark.parametrize("single", [False, True], ids=["two_kernels", "single_launch"])
+def test_sixty_four_groups_graph_replays_equal_regular_steps(single):
+    # The device group table at the group limit: every group's constants and
+    # step count, derived on the device, match the host's for regular steps.
+    _regular_vs_graph(sixty_four_groups(), tuple(1000 * q + 1 for q in range(64)),
+                      single_launch=None if single else 0)
+
+
+def _regular_vs_graph(w, resume, single_launch=None):
     finals, norms = [], []
     for graph_mode in (False, True):
         params = W.draw_params(w, "cpu")
         dl = DeviceList(w, params)
         opt = make_opt(w)
+        if single_launch is not None:
+            opt.set_single_launch(single_launch)
         for q, t in enumerate(resume):
             opt.set_group_step(q, t)
         stream = torch.cuda.Stream()
@@ -123,7 +136,9 @@ def test_graph_replays_equal_regular_steps_bit_for_bit(group_div):
         torch.cuda.synchronize()
         if graph_mode:
             opt.pull_groups(stream)
-        assert [opt.get_group_step(q) for q in range(len(w.groups))] == [t + w.steps for t in resume]
+        stepped = [any(t.trainable and t.group == q for t in w.tensors) for q in range(len(w.groups))]
+        assert ([opt.get_group_step(q) for q in range(len(w.groups))] ==
+                [t + (w.steps if stepped[q] else 0) for q, t in enumerate(resume)])
         finals.append([x.cpu().view(torch.int32) for x in dl.p + dl.m + dl.v])
         norms.append(got)
         del graph

@@ -10,8 +10,8 @@ import torch
 import golden_fixture
 import workloads as W
 from parity_harness import (ATOL, NORM_RTOL, RTOL, DeviceList, assert_close, make_opt, make_oracle,
-                            run_parity)
-from tensor_grad_clip_gb300 import SomaOpt, TensorList, build
+                            run_parity, sixty_four_groups)
+from tensor_grad_clip_gb300 import SomaOpt, TensorList, _abi, build
 
 pytestmark = pytest.mark.gpu
 
@@ -149,6 +149,15 @@ def test_edge_shapes_mixed_dtypes_and_groups():
     w = _custom(tensors, groups, steps=3)
     run_parity(w)
     run_parity(w, frozen_null=True, tuning=dict(update_chunk=64, norm_chunk=64))
+
+
+@pytest.mark.parametrize("single", [False, True], ids=["two_kernels", "single_launch"])
+def test_sixty_four_groups(single):
+    # Group ids up to the limit: each group's constants reach its tensors,
+    # on the two-kernel path and in the single-launch step.
+    w = sixty_four_groups()
+    assert len(w.groups) == _abi.SOMA_MAX_GROUPS
+    run_parity(w, single_launch=None if single else 0, expect_launches=1 if single else 2)
 
 
 def test_nothing_owned_and_all_frozen():
