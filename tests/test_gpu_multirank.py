@@ -106,3 +106,44 @@ def test_local_sum_is_the_owned_square_sum():
     for q in range(len(w.groups)):
         assert opt.get_group_step(q) == 0  # the local sum alone is not a step
     opt.close()
+
+
+def test_rank_sums_up_to_the_limit_are_added_in_rank_order():
+    # soma_opt_step_from_sumsq with SOMA_MAX_RANKS per-rank sums (this rank's
+    # own square-sum at one index, the others drawn): the norm is the square
+    # root of their fp64 sum taken in index order, bit for bit (one add chain
+    # and a correctly rounded square root on both sides), c is the oracle's
+    # coefficient of that norm, and every tensor is updated with that c.
+    import oracle
+    from tensor_grad_clip_gb300 import _abi
+    w = W.with_steps(W.SMALL["tiny"](), 1)
+    params = W.draw_params(w, "cpu")
+    grads = W.draw_grads(w, 1, "cpu")
+    dl = DeviceList(w, params)
+    dl.load_grads(grads)
+    opt = make_opt(w)
+    n = _abi.SOMA_MAX_RANKS
+    parts = torch.rand(n, generator=torch.Generator().manual_seed(11), dtype=torch.float64) * 0.5
+    local = torch.zeros(1, dtype=torch.float64, device="cuda")
+    opt.sumsq(dl.tl, w.grad_divisor, local)
+    parts[n // 3] = local.item()
+    opt.step_from_sumsq(dl.tl, w.grad_divisor, w.max_norm, parts.cuda())
+    norm, coef, nonfinite = opt.get_norm()
+    total = 0.0
+    for x in parts.tolist():
+        total += x
+    assert not nonfinite
+    assert norm == math.sqrt(total)
+    assert coef == oracle.clip_coef(math.sqrt(total), w.max_norm) < 1.0
+    q = w.groups[0]
+    for k, t in enumerate(w.tensors):
+        if not t.trainable:
+            continue
+        p = params[k].double().numpy().reshape(-1).copy()
+        m, v = np.zeros_like(p), np.zeros_like(p)
+        oracle.adamw_update(p, grads[k], m, v, lr=q.lr, beta1=q.beta1, beta2=q.beta2, eps=q.eps,
+                            weight_decay=q.weight_decay, step=1, c=coef, divisor=w.grad_divisor)
+        assert_close(f"{t.name} p", dl.p[k].cpu().numpy(), p)
+        assert_close(f"{t.name} m", dl.m[k].cpu().numpy(), m)
+        assert_close(f"{t.name} v", dl.v[k].cpu().numpy(), v)
+    opt.close()
