@@ -143,3 +143,35 @@ def test_oversized_list_is_refused_before_any_work():
     torch.cuda.synchronize()
     assert out.cpu().tolist() == [-1.0, -1.0]  # nothing was enqueued
     assert _abi.soma_clip_norm_noalloc(0, None, 0, 1.0, 1.0, None, stream) == _abi.SOMA_ERR_INVALID_ARG
+
+
+def test_list_near_the_scratch_capacity():
+    # 60 000 small fp32 entries (1-17 elements each, at odd element offsets
+    # in one buffer, a tenth of them not owned): 54 000 owned segments of 64
+    # bytes, about 3.5 MB of tables in the 4 MiB array, staged by about 115
+    # copy launches.  The norm and c match the oracle's sum over the owned
+    # entries in list order.
+    import numpy as np
+    n = 60_000
+    rng = np.random.default_rng(5)
+    sizes = rng.integers(1, 18, n)
+    offs = np.cumsum(np.concatenate([[0], (sizes + rng.integers(0, 4, n))[:-1]]))
+    owned = rng.random(n) > 0.1
+    g_cpu = torch.randn(int(offs[-1] + sizes[-1]), generator=torch.Generator().manual_seed(6))
+    g = g_cpu.cuda()
+    arr = (_abi.soma_tensor_t * n)()
+    base = g.data_ptr()
+    for k in range(n):
+        e = arr[k]
+        e.param = e.exp_avg = e.exp_avg_sq = e.grad = base + 4 * int(offs[k])
+        e.numel, e.group, e.grad_dtype, e.trainable, e.owned = int(sizes[k]), 0, _abi.SOMA_DTYPE_F32, 1, int(owned[k])
+    out = torch.full((2,), float("nan"), dtype=torch.float64, device="cuda")
+    divisor, max_norm = 4.0, 1.0
+    st = _abi.soma_clip_norm_noalloc(0, ctypes.cast(arr, ctypes.POINTER(_abi.soma_tensor_t)), n, divisor, max_norm,
+                                     out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == _abi.SOMA_OK
+    got_norm, got_coef = out.cpu().tolist()
+    idx = np.concatenate([np.arange(o, o + s) for o, s, w in zip(offs, sizes, owned) if w])
+    rn = math.sqrt(oracle.tensor_sqsum(g_cpu.numpy()[idx], divisor))
+    assert math.isclose(got_norm, rn, rel_tol=NORM_RTOL), (got_norm, rn)
+    assert math.isclose(got_coef, oracle.clip_coef(rn, max_norm), rel_tol=NORM_RTOL)
