@@ -18,7 +18,6 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, os.path.dirname(os.path.dirname(HERE)))
 
-import oracle  # noqa: E402
 from oracle import GroupState, OracleOptimizer  # noqa: E402
 
 OUT = os.path.join(HERE, "three_tensor_steps.txt")

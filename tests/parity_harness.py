@@ -15,7 +15,6 @@ import math
 import numpy as np
 import torch
 
-import oracle
 import workloads as W
 from oracle import GroupState, OracleOptimizer
 from tensor_grad_clip_gb300 import SomaOpt, TensorList

@@ -4,13 +4,12 @@ oracle after every replay; plus the rules that keep a captured graph valid."""
 import math
 from dataclasses import replace
 
-import numpy as np
 import pytest
 import torch
 
 import workloads as W
 from parity_harness import NORM_RTOL, DeviceList, assert_close, make_opt, make_oracle, sixty_four_groups
-from tensor_grad_clip_gb300 import SomaError, TensorList, _abi, build
+from tensor_grad_clip_gb300 import SomaError, _abi, build
 
 pytestmark = pytest.mark.gpu
 

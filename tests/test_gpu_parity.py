@@ -9,8 +9,8 @@ import torch
 
 import golden_fixture
 import workloads as W
-from parity_harness import (ATOL, NORM_RTOL, RTOL, DeviceList, assert_close, make_opt, make_oracle,
-                            run_parity, sixty_four_groups)
+from parity_harness import (NORM_RTOL, DeviceList, assert_close, make_opt, make_oracle, run_parity,
+                            sixty_four_groups)
 from tensor_grad_clip_gb300 import SomaOpt, TensorList, _abi, build
 
 pytestmark = pytest.mark.gpu

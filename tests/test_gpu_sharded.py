@@ -97,7 +97,6 @@ def _run(world, backend, tmp_path):
 
 
 def _check_against_whole_model(res, world):
-    import oracle
     import workloads as W
     from parity_harness import NORM_RTOL, assert_close
     from oracle import GroupState, OracleOptimizer

@@ -11,7 +11,6 @@ import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
 
-import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
